@@ -1,0 +1,399 @@
+#!/usr/bin/env python
+"""Benchmark of the Lightning Attention forward on B300.
+
+One step = one prefill of the 64-head, 8192-token workload (B=1, H=64, N=8192, d=128,
+bf16 I/O, fp32 state) through ``la_prefill``, inputs already resident in HBM.  The
+inputs (4 x 128 MiB) plus output (128 MiB) are larger than the 126 MB L2, so no flush
+is needed between steps.  Printed as one JSON line:
+
+* ``value``: prefill tokens/s over all ranks (each rank runs its own independent
+  sequence: weak scaling, no collective on the data path)
+* ``tflops_alg``: 4 B H N d^2 / time, and its fraction of the measured bf16 peak
+* ``roofline``: the dominant kernel's algorithmic bytes / its measured duration
+  against the measured HBM copy bandwidth
+* ``decode``: the batched decode workload (B=256, H=64, d=128, fp32 state), GB/s
+* ``e2e``: the same prefill with pinned host inputs, the H2D copies and the D2H
+  copy of the output inside the timed region
+* ``cpu_baseline``: the fp64 oracle on a bounded sample, on this host's cores
+
+``--impl reference`` times the oracle instead (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("prefill tokens/s & TFLOP/s (H=64,d=128) as % bf16 peak; decode GB/s % HBM")
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+# ----------------------------------------------------------------------------- helpers
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="prefill_8k")
+    ap.add_argument("--simt", action="store_true", help="time the CUDA-core prefill kernel")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle sample")
+    a = ap.parse_args(argv)
+    a.warmup = max(a.warmup, 3)
+    return a
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(backend):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return rank, world
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax = float(r[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_traffic(kernel: str, source_files):
+    """dram bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel source (the summary records the sources' sha256)."""
+    h = hashlib.sha256()
+    for p in source_files:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    digest = h.hexdigest()[:16]
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.txt")
+    if not os.path.exists(path):
+        return None, digest
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("source_sha256_16") != digest:
+        return None, digest
+    try:
+        return float(vals["dram_bytes_per_launch"]), digest
+    except (KeyError, ValueError):
+        return None, digest
+
+
+# ----------------------------------------------------------------------------- oracle arm
+def oracle_sample(w, seconds: float, seed_offset: int = 0):
+    """Time the fp64 oracle on the first n tokens of the workload (all heads), n chosen
+    so one run takes about ``seconds``.  Returns (tokens/s, n, threads, secs)."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    rng = np.random.default_rng(w.seed + seed_offset)
+    threads = os.cpu_count() or 1
+
+    def run(n):
+        q, k, v, g = (rng.standard_normal((w.B, n, w.H, w.d)) * w.scale for _ in range(4))
+        t0 = time.perf_counter()
+        oracle.prefill(q, k, v, g, nthreads=threads)
+        return time.perf_counter() - t0
+
+    n = 64
+    t = run(n)
+    while t < seconds / 4 and n < w.N:
+        n = min(w.N, n * 4)
+        t = run(n)
+    if t < seconds and n < w.N:
+        n = min(w.N, max(n, int(n * seconds / max(t, 1e-3))))
+        t = run(n)
+    used = min(threads, w.B * w.H)
+    return w.B * n / t, n, used, t
+
+
+def run_reference(a):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from linear_attention_hybrid_fwd_b300.inputs import WORKLOADS
+    w = WORKLOADS[a.workload]
+    tps, n, used, secs = oracle_sample(w, min(a.cpu_seconds, 4.0))
+    # each step: the same bounded sample; warm-up runs untimed
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(w.seed)
+    q, k, v, g = (rng.standard_normal((w.B, n, w.H, w.d)) * w.scale for _ in range(4))
+    for _ in range(a.warmup):
+        oracle.prefill(q, k, v, g, nthreads=used)
+    t0 = time.perf_counter()
+    for _ in range(a.steps):
+        oracle.prefill(q, k, v, g, nthreads=used)
+    dt = (time.perf_counter() - t0) / a.steps
+    value = w.B * n / dt
+    sample = f"first {n} of {w.N} tokens, all {w.H} heads, B={w.B}, fp64"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": a.steps, "warmup": a.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "sample_tokens": n},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+def time_steps(torch, fn, steps, stream):
+    """CUDA events on ``stream`` around each step; returns per-step ms list."""
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    evs[0].record(stream)
+    for i in range(steps):
+        fn()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
+
+
+def run_ours(a):
+    import torch
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dist_init("nccl")
+    dev = torch.device("cuda", local)
+    from linear_attention_hybrid_fwd_b300 import build as la_build
+    la_build.build()
+    import linear_attention_hybrid_fwd_b300 as la
+    from linear_attention_hybrid_fwd_b300.inputs import (WORKLOADS, make_decode_inputs,
+                                                         make_prefill_inputs)
+    peaks, peak_src = load_peaks()
+    w = WORKLOADS[a.workload]
+    stream = torch.cuda.current_stream(dev)
+
+    q, k, v, g = make_prefill_inputs(w.B, w.N, w.H, w.d, torch.bfloat16, w.scale,
+                                     w.seed + 100 * rank, dev)
+    out = torch.empty_like(q)
+    S = torch.empty((w.B, w.H, w.d, w.d), device=dev, dtype=torch.float32)
+
+    def step():
+        la.la_prefill(q, k, v, g, out=out, kv_state_out=S, simt=a.simt)
+
+    for _ in range(a.warmup):
+        step()
+    torch.cuda.synchronize()
+    if la.la_get_device_status() != 0:
+        raise SystemExit("device status error after warm-up")
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    n0 = la.la_launch_count()
+    per_step = time_steps(torch, step, a.steps, stream)
+    launches = la.la_launch_count() - n0
+    barrier()
+    clk = clocks.stop()
+    ms_local = sum(per_step) / len(per_step)
+    ms = max_over_ranks(ms_local, dev)
+    tokens = w.B * w.N
+    value = tokens * world / (ms / 1e3)
+    flops = 4.0 * w.B * w.H * w.N * w.d * w.d
+    tflops = flops / (ms / 1e3) / 1e12
+    io_bytes = 5.0 * w.B * w.N * w.H * w.d * 2 + w.B * w.H * w.d * w.d * 4
+    # the dominant kernel is the whole step on the tensor-core path (one kernel
+    # after a small counter reset); its duration is the per-step event time
+    kern = "la_prefill_simt" if a.simt else "la_prefill_tc"
+    src = [os.path.join(ROOT, "linear_attention_hybrid_fwd_b300", "csrc", f)
+           for f in ("la_simt.cu",) if a.simt] or [
+        os.path.join(ROOT, "linear_attention_hybrid_fwd_b300", "csrc", "la_prefill_tc.cu")]
+    traffic, digest = kernel_traffic(kern, src)
+    achieved = io_bytes / (ms_local / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "io": "bf16 q,k,v,g,out; fp32 state", "l2": "inputs larger than L2",
+                   "parallelism": f"replicas x{world} (independent sequences)",
+                   "kernel": "cuda-core" if a.simt else "tensor-core"},
+        "tflops_alg": tflops, "tflops_alg_frac_bf16_peak": tflops / peaks["bf16_tflops"],
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": traffic, "kernel": kern, "peak_source": peak_src,
+                     "alg_bytes_per_launch": io_bytes, "source_sha256_16": digest},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+
+    if not a.no_decode:
+        line["decode"] = bench_decode(a, torch, la, WORKLOADS["decode_b256"], dev, stream,
+                                      peaks, make_decode_inputs, rank)
+    if not a.no_e2e:
+        line["e2e"] = bench_e2e(a, torch, la, q, k, v, g, out, S, stream, world, dev)
+    del q, k, v, g, out
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        tps, n, used, secs = oracle_sample(w, a.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": tps, "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "sample": f"first {n} of {w.N} tokens, all {w.H} heads, fp64, {secs:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    barrier()
+    return 0
+
+
+def bench_decode(a, torch, la, w, dev, stream, peaks, make_decode_inputs, rank):
+    """Decode GB/s: state read + write (fp32) plus q,k,v,g,out (bf16) per step."""
+    gen = torch.Generator(device=dev).manual_seed(w.seed + rank)
+    S = torch.randn((w.B, w.H, w.d, w.d), generator=gen, device=dev) * 0.1
+    ins = [make_decode_inputs(w.B, w.H, w.d, torch.bfloat16, w.scale, w.seed, s, dev)
+           for s in range(4)]
+    out = torch.empty_like(ins[0][0])
+    it = [0]
+
+    def step():
+        qq, kk, vv, gg = ins[it[0] % 4]
+        it[0] += 1
+        la.la_decode_step(S, qq, kk, vv, gg, out=out)
+
+    for _ in range(max(a.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    n0 = la.la_launch_count()
+    per = time_steps(torch, step, max(a.steps, 10), stream)
+    launches = la.la_launch_count() - n0
+    ms = sum(per) / len(per)
+    nbytes = 2.0 * w.B * w.H * w.d * w.d * 4 + 5.0 * w.B * w.H * w.d * 2
+    gbs = nbytes / (ms / 1e3) / 1e9
+    del S, ins
+    return {"workload": w.name, "B": w.B, "H": w.H, "d": w.d, "ms_per_step": ms,
+            "bytes_per_step": nbytes, "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
+            "tokens_per_s": w.B / (ms / 1e3), "gpu_launches_per_step": launches / len(per)}
+
+
+def bench_e2e(a, torch, la, q, k, v, g, out, S, stream, world, dev):
+    """Through the public API with host buffers: pinned H2D of q,k,v,g, la_prefill,
+    D2H of out, all inside the timed region."""
+    hq, hk, hv, hg = (t.cpu().pin_memory() for t in (q, k, v, g))
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def step():
+        for h, d in ((hq, q), (hk, k), (hv, v), (hg, g)):
+            d.copy_(h, non_blocking=True)
+        la.la_prefill(q, k, v, g, out=out, kv_state_out=S, simt=a.simt)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    steps = max(3, min(a.steps, 10))
+    barrier()
+    t0 = time.perf_counter()
+    per = time_steps(torch, step, steps, stream)
+    wall = (time.perf_counter() - t0) / steps
+    ms = max_over_ranks(max(sum(per) / len(per), wall * 1e3), dev)
+    tokens = q.shape[0] * q.shape[1]
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg))
+    d2h = hout.numel() * hout.element_size()
+    return {"value": tokens * world / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def main(argv=None):
+    a = parse_args(argv)
+    if a.impl == "reference":
+        return run_reference(a)
+    return run_ours(a)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

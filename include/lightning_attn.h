@@ -1,0 +1,125 @@
+/*
+ * lightning_attn.h -- C ABI of liblightning_attn.so, the B300 (sm_103a) forward pass
+ * of the Lightning Attention layer (causal linear attention with an RMSNorm output
+ * and a sigmoid gate).
+ *
+ * The operation (MiniMax-01 deep dive, Hugging Face blog, "Hybrid Modeling", the
+ * four-step mechanism of the 7/8 linear-attention layers):
+ *   q^ = SiLU(q), k^ = SiLU(k), v^ = SiLU(v)                       (step 2)
+ *   S_t = S_{t-1} + k^_t^T v^_t ,  y_t = q^_t S_t   (causal, s <= t) (step 3, the
+ *         O(d^2 n) right-product route the same section contrasts with O(n^2 d))
+ *   out_t = y_t / sqrt(mean(y_t^2) + eps) * sigmoid(g_t)           (step 4)
+ * The mean runs over all H*d features of a token; the RMSNorm weight is one; g is
+ * the gate input and gets no SiLU; there is no 1/sqrt(d) scale and no decay.
+ * Head count and head size come from the MiniMax-Text-01 architecture list
+ * (64 heads of size 128); this library requires d == 128.
+ *
+ * Layouts (all row-major, no padding):
+ *   prefill q, k, v, g, out, y_debug : [B][N][H][d]   (= [B*N][H*d])
+ *   decode  q, k, v, g, out          : [B][H][d]
+ *   state   kv_state                 : [B][H][d][d] fp32, S[i][j] = sum_s k^_s[i] v^_s[j]
+ *
+ * Ownership and memory: every pointer is a DEVICE pointer owned by the caller
+ * (16-byte aligned).  Inputs are read only and are not modified; out must not alias
+ * an input.  The library owns one internal per-device workspace (exchange buffers,
+ * status word), grown on demand under a mutex and freed at unload.
+ *
+ * Execution: calls enqueue kernels on the given CUDA stream (NULL = legacy default
+ * stream) and return without synchronising.  Calls on one device share the
+ * workspace, so calls that may run concurrently on different streams of the same
+ * device must be ordered by the caller.  Argument errors are detected on the
+ * host before anything is launched and nothing is written.  A kernel that gives up
+ * a bounded wait records LA_ERR_TIMEOUT in the device status word, which
+ * la_get_device_status() reads.  Nothing in the library prints, exits or traps.
+ */
+#ifndef LIGHTNING_ATTN_H
+#define LIGHTNING_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LA_OK = 0,
+    LA_ERR_INVALID_ARG = 1, /* NULL pointer, B/H/N out of range, eps < 0, aliasing   */
+    LA_ERR_UNSUPPORTED = 2, /* d != 128, or a shape the kernels do not cover          */
+    LA_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned                       */
+    LA_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed            */
+    LA_ERR_NOMEM = 5,       /* the workspace could not be grown                       */
+    LA_ERR_TIMEOUT = 6      /* a kernel gave up a bounded cross-CTA wait              */
+} la_status;
+
+typedef enum {
+    LA_BF16 = 0, /* bf16 inputs/outputs, fp32 state and accumulation */
+    LA_F32 = 1   /* fp32 inputs/outputs, fp32 everywhere              */
+} la_dtype;
+
+/* Flags for the _ex entry points. */
+#define LA_FLAG_SIMT 1u /* prefill: run the CUDA-core kernel instead of the
+                           tensor-core kernel (the only kernel for LA_F32) */
+
+/*
+ * Prefill of B sequences of N tokens ("Hybrid Modeling", mechanism steps 2-4).
+ * bf16 I/O, eps = 1e-6, zero initial state, legacy default stream.
+ *   q, k, v, g    in  [B][N][H][d] bf16, pre-activation projections
+ *   out           out [B][N][H][d] bf16
+ *   kv_state_out  out [B][H][d][d] fp32, the state after token N-1 (may be NULL)
+ * N == 0 is legal: kv_state_out receives zeros and out is untouched.
+ * Returns an la_status.
+ */
+int la_prefill(const void* q, const void* k, const void* v, const void* g, void* out,
+               float* kv_state_out, int B, int H, int64_t N, int d);
+
+/*
+ * One decode step for B sequences: for each (b,h), S += k^T v (in place), then
+ * y = q S; out = RMSNorm over the H*d features of each b, times sigmoid(g).
+ * bf16 I/O, eps = 1e-6, legacy default stream.
+ *   kv_state  in/out [B][H][d][d] fp32
+ *   q,k,v,g   in     [B][H][d] bf16;  out  out [B][H][d] bf16
+ */
+int la_decode_step(float* kv_state, const void* q, const void* k, const void* v,
+                   const void* g, void* out, int B, int H, int d);
+
+/*
+ * Extended prefill.
+ *   kv_state_in  in  [B][H][d][d] fp32 initial state, or NULL for zeros; lets a long
+ *                    sequence be processed in pieces (the state is the resume point)
+ *   kv_state_out out [B][H][d][d] fp32 or NULL; may equal kv_state_in
+ *   y_debug      out [B][N][H][d] fp32 pre-norm y, or NULL
+ *   dtype        la_dtype of q, k, v, g, out
+ *   eps          RMSNorm epsilon (>= 0)
+ *   flags        LA_FLAG_* bits
+ *   cuda_stream  cudaStream_t to enqueue on (NULL = legacy default stream)
+ */
+int la_prefill_ex(const void* q, const void* k, const void* v, const void* g, void* out,
+                  float* kv_state_out, const float* kv_state_in, float* y_debug, int B,
+                  int H, int64_t N, int d, int dtype, float eps, unsigned flags,
+                  void* cuda_stream);
+
+/* Extended decode step: as la_decode_step with dtype, eps, an optional fp32 pre-norm
+   y_debug [B][H][d] (or NULL) and a stream. */
+int la_decode_step_ex(float* kv_state, const void* q, const void* k, const void* v,
+                      const void* g, void* out, float* y_debug, int B, int H, int d,
+                      int dtype, float eps, void* cuda_stream);
+
+/* Static text for an la_status value. */
+const char* la_status_string(int status);
+
+/* Synchronises cuda_stream, returns and clears the device status word of the current
+   device (LA_OK or LA_ERR_TIMEOUT), or LA_ERR_CUDA if synchronisation failed. */
+int la_get_device_status(void* cuda_stream);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int la_version(void);
+
+/* Number of kernels this library has launched in this process (all devices), for
+   launch accounting by benchmarks.  Counts launches, not completed work. */
+int64_t la_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIGHTNING_ATTN_H */

@@ -1,0 +1,182 @@
+"""Lightning Attention forward on B300 (sm_103a): a thin ctypes binding.
+
+This module only marshals arguments to ``liblightning_attn.so`` (the C ABI declared in
+``include/lightning_attn.h``): torch tensors become device pointers, torch's current
+CUDA stream becomes the ``cudaStream_t``.  Every step of the computation runs in the
+library's CUDA kernels.  There is no other implementation: if the library is missing
+or no CUDA device is present, the calls raise.
+
+Functions carry the C names:
+
+* ``la_prefill(q, k, v, g, ...)``       -- prefill of ``[B, N, H, d]`` inputs
+* ``la_decode_step(kv_state, q, ...)``  -- one token per sequence, ``[B, H, d]`` inputs
+* ``la_status_string``, ``la_get_device_status``, ``la_version``
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = ["la_prefill", "la_decode_step", "la_status_string", "la_get_device_status",
+           "la_version", "la_launch_count", "LaError", "library_path", "load_library", "LA_BF16", "LA_F32",
+           "LA_FLAG_SIMT"]
+
+LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_MISALIGNED = 0, 1, 2, 3
+LA_ERR_CUDA, LA_ERR_NOMEM, LA_ERR_TIMEOUT = 4, 5, 6
+LA_BF16, LA_F32 = 0, 1
+LA_FLAG_SIMT = 1
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "liblightning_attn.so")
+_lib = None
+
+
+class LaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {la_status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load ``liblightning_attn.so`` (built in-tree by ``build.py``); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(
+            f"{_LIB_PATH} is missing: run `python -m linear_attention_hybrid_fwd_b300.build`")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, fp, i32, i64, f32, u32 = (ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                  ctypes.c_int64, ctypes.c_float, ctypes.c_uint)
+    lib.la_prefill.argtypes = [vp, vp, vp, vp, vp, fp, i32, i32, i64, i32]
+    lib.la_prefill.restype = i32
+    lib.la_prefill_ex.argtypes = [vp, vp, vp, vp, vp, fp, fp, fp, i32, i32, i64, i32, i32, f32,
+                                  u32, vp]
+    lib.la_prefill_ex.restype = i32
+    lib.la_decode_step.argtypes = [fp, vp, vp, vp, vp, vp, i32, i32, i32]
+    lib.la_decode_step.restype = i32
+    lib.la_decode_step_ex.argtypes = [fp, vp, vp, vp, vp, vp, fp, i32, i32, i32, i32, f32, vp]
+    lib.la_decode_step_ex.restype = i32
+    lib.la_status_string.argtypes = [i32]
+    lib.la_status_string.restype = ctypes.c_char_p
+    lib.la_get_device_status.argtypes = [vp]
+    lib.la_get_device_status.restype = i32
+    lib.la_version.argtypes = []
+    lib.la_version.restype = i32
+    lib.la_launch_count.argtypes = []
+    lib.la_launch_count.restype = ctypes.c_int64
+    _lib = lib
+    return lib
+
+
+def la_status_string(status: int) -> str:
+    return load_library().la_status_string(int(status)).decode()
+
+
+def la_version() -> int:
+    return load_library().la_version()
+
+
+def la_launch_count() -> int:
+    return load_library().la_launch_count()
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def la_get_device_status(stream=None) -> int:
+    return load_library().la_get_device_status(_stream_handle(stream))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return LA_BF16
+    if t.dtype == torch.float32:
+        return LA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: expected bfloat16 or float32")
+
+
+def _check(ts, names):
+    import torch
+    dev = None
+    for t, n in zip(ts, names):
+        if t is None:
+            continue
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{n} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{n} is on {t.device}, expected {dev}")
+
+
+def la_prefill(q, k, v, g, out=None, kv_state_out=None, kv_state_in=None, y_debug=None,
+               eps: float = 1e-6, simt: bool = False, want_state: bool = True, stream=None):
+    """Prefill. ``q, k, v, g``: ``[B, N, H, d]`` (bf16 or fp32, contiguous, CUDA).
+
+    Returns ``(out, kv_state_out)``; ``kv_state_out`` is ``[B, H, d, d]`` fp32 (``None``
+    when ``want_state`` is False and none was passed).  ``kv_state_in`` continues a
+    sequence from a previous state; ``y_debug`` (fp32 ``[B, N, H, d]``) receives the
+    pre-norm output.  ``simt`` selects the CUDA-core kernel.
+    """
+    import torch
+    B, N, H, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if kv_state_out is None and want_state:
+        kv_state_out = torch.empty((B, H, d, d), device=q.device, dtype=torch.float32)
+    _check([q, k, v, g, out, kv_state_out, kv_state_in, y_debug],
+           ["q", "k", "v", "g", "out", "kv_state_out", "kv_state_in", "y_debug"])
+    for t, n in ((k, "k"), (v, "v"), (g, "g"), (out, "out")):
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{n} must match q in shape and dtype")
+    for t, n in ((kv_state_out, "kv_state_out"), (kv_state_in, "kv_state_in")):
+        if t is not None and (t.shape != (B, H, d, d) or t.dtype != torch.float32):
+            raise ValueError(f"{n} must be float32 [B, H, d, d]")
+    if y_debug is not None and (y_debug.shape != q.shape or y_debug.dtype != torch.float32):
+        raise ValueError("y_debug must be float32 [B, N, H, d]")
+    rc = load_library().la_prefill_ex(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out), _ptr(kv_state_out), _ptr(kv_state_in),
+        _ptr(y_debug), B, H, N, d, _dtype_code(q), float(eps), LA_FLAG_SIMT if simt else 0,
+        _stream_handle(stream))
+    if rc != LA_OK:
+        raise LaError(rc, "la_prefill")
+    return out, kv_state_out
+
+
+def la_decode_step(kv_state, q, k, v, g, out=None, y_debug=None, eps: float = 1e-6,
+                   stream=None):
+    """One decode step. ``kv_state`` ``[B, H, d, d]`` fp32 is updated in place;
+    ``q, k, v, g`` are ``[B, H, d]``.  Returns ``out`` (``[B, H, d]``, dtype of q)."""
+    import torch
+    B, H, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check([kv_state, q, k, v, g, out, y_debug],
+           ["kv_state", "q", "k", "v", "g", "out", "y_debug"])
+    for t, n in ((k, "k"), (v, "v"), (g, "g"), (out, "out")):
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{n} must match q in shape and dtype")
+    if kv_state.shape != (B, H, d, d) or kv_state.dtype != torch.float32:
+        raise ValueError("kv_state must be float32 [B, H, d, d]")
+    rc = load_library().la_decode_step_ex(
+        _ptr(kv_state), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out), _ptr(y_debug), B, H, d,
+        _dtype_code(q), float(eps), _stream_handle(stream))
+    if rc != LA_OK:
+        raise LaError(rc, "la_decode_step")
+    return out

@@ -1,0 +1,219 @@
+// la_api.cu -- the C ABI of liblightning_attn.so (declared in include/lightning_attn.h):
+// argument validation, the per-device workspace, and launch sequencing on the
+// caller's stream.  Every numeric step runs in the CUDA kernels of la_simt.cu and
+// la_prefill_tc.cu; nothing here computes on the host.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "../../include/lightning_attn.h"
+#include "la_internal.h"
+
+namespace la {
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int64_t> g_launches{0};
+std::mutex g_ws_mutex;
+Workspace g_ws[kMaxDevices];
+
+struct WorkspaceReaper {
+    ~WorkspaceReaper() {
+        // Process teardown: the driver may already be gone; ignore errors.
+        for (auto& w : g_ws) {
+            if (w.base) cudaFree(w.base);
+            if (w.status) cudaFree(w.status);
+        }
+    }
+} g_reaper;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
+
+}  // namespace
+
+void note_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+int workspace_acquire(size_t bytes, Workspace* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    Workspace& w = g_ws[dev];
+    if (!w.status) {
+        if (cudaMalloc(&w.status, 256) != cudaSuccess) return LA_ERR_NOMEM;
+        if (cudaMemset(w.status, 0, 256) != cudaSuccess) return LA_ERR_CUDA;
+    }
+    if (bytes > w.bytes) {
+        // cudaFree waits for work already queued on the device, so a smaller
+        // workspace still in use by an earlier call is not released under it.
+        if (w.base) cudaFree(w.base);
+        w.base = nullptr;
+        w.bytes = 0;
+        const size_t want = (bytes + (size_t(1) << 21) - 1) & ~((size_t(1) << 21) - 1);
+        if (cudaMalloc(&w.base, want) != cudaSuccess) {
+            cudaGetLastError();
+            return LA_ERR_NOMEM;
+        }
+        w.bytes = want;
+    }
+    *out = w;
+    return LA_OK;
+}
+
+}  // namespace la
+
+using namespace la;
+
+extern "C" {
+
+const char* la_status_string(int s) {
+    switch (s) {
+        case LA_OK: return "ok";
+        case LA_ERR_INVALID_ARG: return "invalid argument";
+        case LA_ERR_UNSUPPORTED: return "unsupported shape (head size must be 128)";
+        case LA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case LA_ERR_CUDA: return "CUDA error";
+        case LA_ERR_NOMEM: return "out of device memory for the workspace";
+        case LA_ERR_TIMEOUT: return "a kernel gave up a bounded cross-CTA wait";
+        default: return "unknown status";
+    }
+}
+
+int la_version(void) { return 100; }
+
+int64_t la_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int la_prefill_ex(const void* q, const void* k, const void* v, const void* g, void* out,
+                  float* kv_state_out, const float* kv_state_in, float* y_debug, int B, int H,
+                  int64_t N, int d, int dtype, float eps, unsigned flags, void* cuda_stream) {
+    // ---- host-side validation: nothing is launched or written on failure ----
+    if (B <= 0 || H <= 0 || N < 0 || d <= 0) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_BF16 && dtype != LA_F32) return LA_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f) || !isfinite(eps)) return LA_ERR_INVALID_ARG;
+    if (flags & ~LA_FLAG_SIMT) return LA_ERR_INVALID_ARG;
+    if (d != kHeadDim) return LA_ERR_UNSUPPORTED;
+    if (B > 65535 || H > 4096) return LA_ERR_UNSUPPORTED;
+    // element counts: B*N*H*d must stay well inside int64 (the kernels index in int64)
+    if (N > (int64_t(1) << 40) / ((int64_t)B * H * d)) return LA_ERR_INVALID_ARG;
+    const bool bf16 = dtype == LA_BF16;
+    const size_t esz = bf16 ? 2 : 4;
+    const int64_t nelem = (int64_t)B * N * H * d;
+    const size_t io_bytes = (size_t)nelem * esz;
+    const size_t state_bytes = (size_t)B * H * d * d * sizeof(float);
+    if (N > 0 && (!q || !k || !v || !g || !out)) return LA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, g, out, kv_state_out, kv_state_in, y_debug};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return LA_ERR_MISALIGNED;
+    if (N > 0) {
+        const void* ins[] = {q, k, v, g};
+        for (const void* p : ins)
+            if (overlaps(out, io_bytes, p, io_bytes)) return LA_ERR_INVALID_ARG;
+        if (overlaps(kv_state_out, state_bytes, out, io_bytes)) return LA_ERR_INVALID_ARG;
+        if (y_debug && overlaps(y_debug, (size_t)nelem * 4, out, io_bytes))
+            return LA_ERR_INVALID_ARG;
+    }
+    if (kv_state_in && kv_state_out && kv_state_in != kv_state_out &&
+        overlaps(kv_state_in, state_bytes, kv_state_out, state_bytes))
+        return LA_ERR_INVALID_ARG;
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
+    if (N == 0) {
+        if (kv_state_out && kv_state_out != kv_state_in) {
+            if (kv_state_in)
+                return cuda_status(cudaMemcpyAsync(kv_state_out, kv_state_in, state_bytes,
+                                                   cudaMemcpyDeviceToDevice, st));
+            return launch_zero_state(kv_state_out, (int64_t)B * H * d * d, st);
+        }
+        return LA_OK;
+    }
+
+    const bool use_tc = bf16 && !(flags & LA_FLAG_SIMT) && prefill_tc_supported(B, H, N) == LA_OK;
+    if (use_tc) {
+        Workspace ws;
+        int rc = workspace_acquire(prefill_tc_workspace_bytes(B, H, N), &ws);
+        if (rc != LA_OK) return rc;
+        return launch_prefill_tc(q, k, v, g, out, kv_state_in, kv_state_out, y_debug, B, H, N,
+                                 eps, ws, st);
+    }
+    // CUDA-core kernel: y in fp32 (into y_debug when given), then the norm/gate pass.
+    float* y = y_debug;
+    if (!y) {
+        Workspace ws;
+        int rc = workspace_acquire((size_t)nelem * sizeof(float), &ws);
+        if (rc != LA_OK) return rc;
+        y = static_cast<float*>(ws.base);
+    }
+    int rc = launch_prefill_simt(q, k, v, kv_state_in, y, kv_state_out, B, H, N, bf16, st);
+    if (rc != LA_OK) return rc;
+    return launch_norm_gate_rows(y, g, out, (int64_t)B * N, H * d, eps, bf16, st);
+}
+
+int la_prefill(const void* q, const void* k, const void* v, const void* g, void* out,
+               float* kv_state_out, int B, int H, int64_t N, int d) {
+    return la_prefill_ex(q, k, v, g, out, kv_state_out, nullptr, nullptr, B, H, N, d, LA_BF16,
+                         1e-6f, 0u, nullptr);
+}
+
+int la_decode_step_ex(float* kv_state, const void* q, const void* k, const void* v,
+                      const void* g, void* out, float* y_debug, int B, int H, int d, int dtype,
+                      float eps, void* cuda_stream) {
+    if (B <= 0 || H <= 0 || d <= 0) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_BF16 && dtype != LA_F32) return LA_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f) || !isfinite(eps)) return LA_ERR_INVALID_ARG;
+    if (d != kHeadDim) return LA_ERR_UNSUPPORTED;
+    if (B > 65535 || H > 65535 || (int64_t)B * H > (int64_t(1) << 31) - 1)
+        return LA_ERR_UNSUPPORTED;
+    if (!kv_state || !q || !k || !v || !g || !out) return LA_ERR_INVALID_ARG;
+    const void* ptrs[] = {kv_state, q, k, v, g, out, y_debug};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return LA_ERR_MISALIGNED;
+    const bool bf16 = dtype == LA_BF16;
+    const size_t io_bytes = (size_t)B * H * d * (bf16 ? 2 : 4);
+    const size_t state_bytes = (size_t)B * H * d * d * sizeof(float);
+    const void* ins[] = {q, k, v, g};
+    for (const void* p : ins) {
+        if (overlaps(out, io_bytes, p, io_bytes)) return LA_ERR_INVALID_ARG;
+        if (overlaps(kv_state, state_bytes, p, io_bytes)) return LA_ERR_INVALID_ARG;
+    }
+    if (overlaps(kv_state, state_bytes, out, io_bytes)) return LA_ERR_INVALID_ARG;
+
+    const size_t ny = (size_t)B * H * d;
+    Workspace ws;
+    int rc = workspace_acquire((ny + (size_t)B * H) * sizeof(float) + 256, &ws);
+    if (rc != LA_OK) return rc;
+    float* y = y_debug ? y_debug : static_cast<float*>(ws.base);
+    float* ss = static_cast<float*>(ws.base) + ny;
+    return launch_decode(kv_state, q, k, v, g, out, y, ss, B, H, eps, bf16,
+                         reinterpret_cast<cudaStream_t>(cuda_stream));
+}
+
+int la_decode_step(float* kv_state, const void* q, const void* k, const void* v,
+                   const void* g, void* out, int B, int H, int d) {
+    return la_decode_step_ex(kv_state, q, k, v, g, out, nullptr, B, H, d, LA_BF16, 1e-6f,
+                             nullptr);
+}
+
+int la_get_device_status(void* cuda_stream) {
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return LA_ERR_CUDA;
+    Workspace ws;
+    int rc = workspace_acquire(0, &ws);
+    if (rc != LA_OK) return rc;
+    int h = 0;
+    if (cudaMemcpy(&h, ws.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return LA_ERR_CUDA;
+    if (h != 0 && cudaMemset(ws.status, 0, sizeof(int)) != cudaSuccess) return LA_ERR_CUDA;
+    return h == 0 ? LA_OK : h;
+}
+
+}  // extern "C"

@@ -1,0 +1,137 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must load on a machine without a CUDA device, export every function that
+``include/lightning_attn.h`` declares, and reject bad arguments on the host before
+anything is launched (these calls never reach the CUDA runtime).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import linear_attention_hybrid_fwd_b300 as la
+from linear_attention_hybrid_fwd_b300 import build as la_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+           if f.endswith(".h")]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    la_build.build()
+    return la.load_library()
+
+
+def _declared_functions():
+    names = set()
+    for h in HEADERS:
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"\b(?:int|int64_t|const char\s*\*|void)\s+(la_\w+)\s*\(", src):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for want in ["la_prefill", "la_decode_step", "la_prefill_ex", "la_decode_step_ex",
+                 "la_status_string", "la_get_device_status", "la_version", "la_launch_count"]:
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert la.la_status_string(s)
+    assert "unknown" in la.la_status_string(99)
+    assert la.la_version() >= 100
+
+
+# Fake, 16-byte aligned, never-dereferenced device addresses: every call below must
+# fail validation on the host, so no pointer is ever touched.
+P = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(8)]
+MIS = ctypes.c_void_p(0x10008)
+
+
+def _prefill(lib, B=1, H=2, N=16, d=128, dtype=la.LA_BF16, eps=1e-6, flags=0, q=None,
+             out=None, ptrs=None):
+    p = list(ptrs or P)
+    if q is not None:
+        p[0] = q
+    if out is not None:
+        p[4] = out
+    return lib.la_prefill_ex(p[0], p[1], p[2], p[3], p[4], p[5], None, None, B, H, N, d, dtype,
+                             eps, flags, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(B=0), la.LA_ERR_INVALID_ARG),
+    (dict(H=0), la.LA_ERR_INVALID_ARG),
+    (dict(N=-1), la.LA_ERR_INVALID_ARG),
+    (dict(d=0), la.LA_ERR_INVALID_ARG),
+    (dict(d=64), la.LA_ERR_UNSUPPORTED),
+    (dict(d=129), la.LA_ERR_UNSUPPORTED),
+    (dict(dtype=7), la.LA_ERR_INVALID_ARG),
+    (dict(eps=-1.0), la.LA_ERR_INVALID_ARG),
+    (dict(eps=float("nan")), la.LA_ERR_INVALID_ARG),
+    (dict(flags=0x100), la.LA_ERR_INVALID_ARG),
+    (dict(q=ctypes.c_void_p(0)), la.LA_ERR_INVALID_ARG),
+    (dict(q=MIS), la.LA_ERR_MISALIGNED),
+    (dict(out=P[0]), la.LA_ERR_INVALID_ARG),           # out aliases q
+    (dict(N=1 << 40), la.LA_ERR_INVALID_ARG),          # element count overflow guard
+])
+def test_prefill_rejects_on_host(lib, kw, want):
+    assert _prefill(lib, **kw) == want
+
+
+def test_prefill_entry_rejects_on_host(lib):
+    assert lib.la_prefill(P[0], P[1], P[2], P[3], P[4], P[5], 1, 2, 16, 64) == \
+        la.LA_ERR_UNSUPPORTED
+    assert lib.la_prefill(None, P[1], P[2], P[3], P[4], P[5], 1, 2, 16, 128) == \
+        la.LA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("args,want", [
+    (dict(B=0), la.LA_ERR_INVALID_ARG),
+    (dict(H=-1), la.LA_ERR_INVALID_ARG),
+    (dict(d=96), la.LA_ERR_UNSUPPORTED),
+    (dict(dtype=3), la.LA_ERR_INVALID_ARG),
+    (dict(state=ctypes.c_void_p(0)), la.LA_ERR_INVALID_ARG),
+    (dict(state=MIS), la.LA_ERR_MISALIGNED),
+    (dict(out=P[1]), la.LA_ERR_INVALID_ARG),           # out aliases q
+])
+def test_decode_rejects_on_host(lib, args, want):
+    a = dict(B=2, H=2, d=128, dtype=la.LA_BF16, state=P[0], out=P[6])
+    a.update(args)
+    rc = lib.la_decode_step_ex(a["state"], P[1], P[2], P[3], P[4], a["out"], None, a["B"],
+                               a["H"], a["d"], a["dtype"], 1e-6, None)
+    assert rc == want
+
+
+def test_decode_entry_rejects_on_host(lib):
+    assert lib.la_decode_step(P[0], P[1], P[2], P[3], P[4], P[5], 1, 1, 32) == \
+        la.LA_ERR_UNSUPPORTED
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """The binding has no other implementation: without the .so it raises."""
+    monkeypatch.setattr(la, "_lib", None)
+    monkeypatch.setattr(la, "_LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(ImportError):
+        la.load_library()
+
+
+def test_package_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "linear_attention_hybrid_fwd_b300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".h", ".cuh")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), f
+                assert "la_oracle" not in src, f

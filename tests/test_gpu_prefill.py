@@ -1,0 +1,176 @@
+"""GPU parity of la_prefill against the fp64 oracle (same seeded input bits).
+
+Covers the tensor-core kernel (bf16 default) and the CUDA-core kernel (fp32 I/O and
+``LA_FLAG_SIMT``), shapes that span several 128-token chunks with ragged tails, the
+64-head 8K-token workload in full, the 128K-token workload on sampled windows plus
+the final state, and the edge cases (N = 0, N = 1, continuation from a state,
+determinism, guard bands).
+"""
+import numpy as np
+import pytest
+
+from parity_util import TOL, host64, rel_max_err, row_rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env(oracle_mod):
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from linear_attention_hybrid_fwd_b300 import build as la_build
+    la_build.build()
+    import linear_attention_hybrid_fwd_b300 as la
+    la.load_library()
+    return torch, la, oracle_mod
+
+
+def _inputs(torch, B, N, H, dtype, scale, seed):
+    from linear_attention_hybrid_fwd_b300.inputs import make_prefill_inputs
+    return make_prefill_inputs(B, N, H, 128, dtype, scale, seed, "cuda")
+
+
+def _check_prefill(env, B, N, H, dt, scale, seed, simt, S0=False):
+    torch, la, orc = env
+    dtype = torch.bfloat16 if dt == "bf16" else torch.float32
+    q, k, v, g = _inputs(torch, B, N, H, dtype, scale, seed)
+    S_in = None
+    if S0:
+        gen = torch.Generator(device="cuda").manual_seed(seed + 99)
+        S_in = torch.randn((B, H, 128, 128), generator=gen, device="cuda") * 0.5
+    y = torch.empty((B, N, H, 128), device="cuda", dtype=torch.float32)
+    out, S = la.la_prefill(q, k, v, g, kv_state_in=S_in, y_debug=y, simt=simt)
+    torch.cuda.synchronize()
+    assert la.la_get_device_status() == 0
+    ref_out, ref_y, ref_S = orc.prefill(host64(q), host64(k), host64(v), host64(g),
+                                        S0=None if S_in is None else host64(S_in))
+    tol = TOL[dt]
+    e_out = rel_max_err(host64(out), ref_out)
+    e_y = row_rel_err(host64(y), ref_y)
+    e_S = rel_max_err(host64(S), ref_S)
+    assert e_out <= tol["out"], f"out rel err {e_out:.3e}"
+    assert e_y <= tol["y_row"], f"y row err {e_y:.3e}"
+    assert e_S <= tol["state"], f"state rel err {e_S:.3e}"
+    assert np.isfinite(host64(out)).all()
+    return e_out, e_y, e_S
+
+
+def test_tiny_f32_workload(env):
+    """fp32 I/O: B1 H1 N512 d128, N(0,1) seed 0, norm over the d features; tol 1e-4."""
+    _check_prefill(env, 1, 512, 1, "f32", 1.0, 0, simt=True)
+
+
+@pytest.mark.parametrize("simt", [False, True])
+@pytest.mark.parametrize("B,N,H", [(1, 1, 1), (1, 127, 2), (2, 300, 4), (1, 1000, 3),
+                                   (3, 129, 8), (1, 257, 64)])
+def test_bf16_shapes(env, B, N, H, simt):
+    _check_prefill(env, B, N, H, "bf16", 0.5, 11 + N + H, simt=simt)
+
+
+@pytest.mark.parametrize("simt", [False, True])
+def test_bf16_with_initial_state(env, simt):
+    _check_prefill(env, 2, 333, 4, "bf16", 0.5, 21, simt=simt, S0=True)
+
+
+def test_f32_shapes(env):
+    _check_prefill(env, 2, 200, 3, "f32", 1.0, 31, simt=True, S0=True)
+
+
+def test_prefill_8k_workload_full(env):
+    """B1 H64 N8192 d128 bf16, inputs N(0,1)*0.5: every output and the final state."""
+    from linear_attention_hybrid_fwd_b300.inputs import WORKLOADS
+    w = WORKLOADS["prefill_8k"]
+    _check_prefill(env, w.B, w.N, w.H, "bf16", w.scale, w.seed, simt=False)
+
+
+def test_prefill_128k_workload_windows(env):
+    """B1 H64 N131072: the oracle runs the state pass up to two seeded 4096-token
+    windows (all heads, since the norm spans them) and checks those windows and the
+    final state."""
+    torch, la, orc = env
+    from linear_attention_hybrid_fwd_b300.inputs import WORKLOADS
+    w = WORKLOADS["prefill_128k"]
+    q, k, v, g = _inputs(torch, w.B, w.N, w.H, torch.bfloat16, w.scale, w.seed)
+    out, S = la.la_prefill(q, k, v, g)
+    torch.cuda.synchronize()
+    assert la.la_get_device_status() == 0
+    rng = np.random.default_rng(w.seed)
+    W = 4096
+    starts = sorted(int(s) for s in rng.integers(0, w.N - W, size=2))
+    S_run = np.zeros((1, w.H, 128, 128))
+    pos = 0
+    slab = 8192
+    for t0 in starts + [w.N]:
+        while pos < t0:  # state-only pass over [pos, t0) in slabs
+            e = min(t0, pos + slab)
+            kh = orc.silu(host64(k[:, pos:e]))
+            vh = orc.silu(host64(v[:, pos:e]))
+            _, S_run = orc.core(kh, kh, vh, S0=S_run, want_y=False)
+            pos = e
+        if t0 == w.N:
+            break
+        sl = slice(t0, t0 + W)
+        ref_out, _, _ = orc.prefill(host64(q[:, sl]), host64(k[:, sl]), host64(v[:, sl]),
+                                    host64(g[:, sl]), S0=S_run)
+        e_out = rel_max_err(host64(out[:, sl]), ref_out)
+        assert e_out <= TOL["bf16"]["out"], f"window {t0}: out rel err {e_out:.3e}"
+    e_S = rel_max_err(host64(S), S_run)
+    assert e_S <= TOL["bf16"]["state"], f"final state rel err {e_S:.3e}"
+
+
+@pytest.mark.parametrize("simt", [False, True])
+def test_split_prefill_continuation(env, simt):
+    """Prefill of [0, N) equals prefill of [0, c) then [c, N) from the carried state."""
+    torch, la, orc = env
+    q, k, v, g = _inputs(torch, 1, 700, 4, torch.bfloat16, 0.5, 41)
+    out, S = la.la_prefill(q, k, v, g, simt=simt)
+    c = 333
+    sl1, sl2 = slice(0, c), slice(c, 700)
+    p = [t[:, sl1].contiguous() for t in (q, k, v, g)]
+    o1, S1 = la.la_prefill(*p, simt=simt)
+    p = [t[:, sl2].contiguous() for t in (q, k, v, g)]
+    o2, S2 = la.la_prefill(*p, kv_state_in=S1, simt=simt)
+    torch.cuda.synchronize()
+    ref = host64(out)
+    assert rel_max_err(np.concatenate([host64(o1), host64(o2)], 1), ref) <= 1e-2
+    assert rel_max_err(host64(S2), host64(S)) <= 1e-5
+
+
+@pytest.mark.parametrize("simt", [False, True])
+def test_deterministic(env, simt):
+    torch, la, _ = env
+    q, k, v, g = _inputs(torch, 1, 600, 8, torch.bfloat16, 0.5, 51)
+    o1, S1 = la.la_prefill(q, k, v, g, simt=simt)
+    o2, S2 = la.la_prefill(q, k, v, g, simt=simt)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(S1, S2)
+
+
+def test_n0_copies_or_zeroes_state(env):
+    torch, la, _ = env
+    q = torch.empty((1, 0, 2, 128), device="cuda", dtype=torch.bfloat16)
+    S_in = torch.randn((1, 2, 128, 128), device="cuda")
+    out, S = la.la_prefill(q, q, q, q, kv_state_in=S_in)
+    torch.cuda.synchronize()
+    assert torch.equal(S, S_in)
+    _, S0 = la.la_prefill(q, q, q, q)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(S0) == 0
+
+
+@pytest.mark.parametrize("simt", [False, True])
+def test_guard_bands_untouched(env, simt):
+    """Outputs written into the middle of larger buffers leave the sentinels intact."""
+    torch, la, _ = env
+    B, N, H, d = 1, 300, 4, 128
+    q, k, v, g = _inputs(torch, B, N, H, torch.bfloat16, 0.5, 61)
+    n = B * N * H * d
+    pad = 4096
+    ob = torch.full((n + 2 * pad,), 7.0, device="cuda", dtype=torch.bfloat16)
+    sb = torch.full((B * H * d * d + 2 * pad,), -3.0, device="cuda", dtype=torch.float32)
+    out = ob[pad:pad + n].view(B, N, H, d)
+    S = sb[pad:pad + B * H * d * d].view(B, H, d, d)
+    la.la_prefill(q, k, v, g, out=out, kv_state_out=S, simt=simt)
+    torch.cuda.synchronize()
+    assert torch.all(ob[:pad] == 7.0) and torch.all(ob[pad + n:] == 7.0)
+    assert torch.all(sb[:pad] == -3.0) and torch.all(sb[-pad:] == -3.0)
