@@ -104,6 +104,13 @@ int la_decode_step_ex(float* kv_state, const void* q, const void* k, const void*
                       const void* g, void* out, float* y_debug, int B, int H, int d,
                       int dtype, float eps, void* cuda_stream);
 
+/* Which prefill kernel la_prefill_ex would run for this shape on the current device:
+   0 = tensor-core kernel, 1 = CUDA-core kernel, or -(la_status) if the arguments are
+   invalid.  The tensor-core kernel covers bf16, d = 128, and B*H no larger than the
+   number of two-CTA clusters the device holds at once (it keeps every head of a
+   token resident for the cross-head RMSNorm). */
+int la_prefill_path(int B, int H, int64_t N, int d, int dtype, unsigned flags);
+
 /* Static text for an la_status value. */
 const char* la_status_string(int status);
 

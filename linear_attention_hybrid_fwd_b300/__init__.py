@@ -10,7 +10,8 @@ Functions carry the C names:
 
 * ``la_prefill(q, k, v, g, ...)``       -- prefill of ``[B, N, H, d]`` inputs
 * ``la_decode_step(kv_state, q, ...)``  -- one token per sequence, ``[B, H, d]`` inputs
-* ``la_status_string``, ``la_get_device_status``, ``la_version``
+* ``la_prefill_path``                  -- which prefill kernel serves a shape
+* ``la_status_string``, ``la_get_device_status``, ``la_version``, ``la_launch_count``
 """
 from __future__ import annotations
 
@@ -18,8 +19,8 @@ import ctypes
 import os
 
 __all__ = ["la_prefill", "la_decode_step", "la_status_string", "la_get_device_status",
-           "la_version", "la_launch_count", "LaError", "library_path", "load_library", "LA_BF16", "LA_F32",
-           "LA_FLAG_SIMT"]
+           "la_version", "la_launch_count", "la_prefill_path", "LaError", "library_path",
+           "load_library", "LA_BF16", "LA_F32", "LA_FLAG_SIMT"]
 
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_MISALIGNED = 0, 1, 2, 3
 LA_ERR_CUDA, LA_ERR_NOMEM, LA_ERR_TIMEOUT = 4, 5, 6
@@ -67,6 +68,8 @@ def load_library():
     lib.la_get_device_status.restype = i32
     lib.la_version.argtypes = []
     lib.la_version.restype = i32
+    lib.la_prefill_path.argtypes = [i32, i32, i64, i32, i32, u32]
+    lib.la_prefill_path.restype = i32
     lib.la_launch_count.argtypes = []
     lib.la_launch_count.restype = ctypes.c_int64
     _lib = lib
@@ -79,6 +82,12 @@ def la_status_string(status: int) -> str:
 
 def la_version() -> int:
     return load_library().la_version()
+
+
+def la_prefill_path(B: int, H: int, N: int, d: int = 128, dtype: int = LA_BF16,
+                    simt: bool = False) -> int:
+    """0 if the tensor-core prefill kernel serves this shape, 1 for the CUDA-core one."""
+    return load_library().la_prefill_path(B, H, N, d, dtype, LA_FLAG_SIMT if simt else 0)
 
 
 def la_launch_count() -> int:

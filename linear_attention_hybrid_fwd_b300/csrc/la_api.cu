@@ -158,6 +158,16 @@ int la_prefill_ex(const void* q, const void* k, const void* v, const void* g, vo
     return launch_norm_gate_rows(y, g, out, (int64_t)B * N, H * d, eps, bf16, st);
 }
 
+int la_prefill_path(int B, int H, int64_t N, int d, int dtype, unsigned flags) {
+    if (B <= 0 || H <= 0 || N < 0 || d <= 0) return -LA_ERR_INVALID_ARG;
+    if (dtype != LA_BF16 && dtype != LA_F32) return -LA_ERR_INVALID_ARG;
+    if (flags & ~LA_FLAG_SIMT) return -LA_ERR_INVALID_ARG;
+    if (d != kHeadDim) return -LA_ERR_UNSUPPORTED;
+    const bool tc = dtype == LA_BF16 && !(flags & LA_FLAG_SIMT) && N > 0 &&
+                    prefill_tc_supported(B, H, N) == LA_OK;
+    return tc ? 0 : 1;
+}
+
 int la_prefill(const void* q, const void* k, const void* v, const void* g, void* out,
                float* kv_state_out, int B, int H, int64_t N, int d) {
     return la_prefill_ex(q, k, v, g, out, kv_state_out, nullptr, nullptr, B, H, N, d, LA_BF16,

@@ -37,7 +37,8 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for want in ["la_prefill", "la_decode_step", "la_prefill_ex", "la_decode_step_ex",
-                 "la_status_string", "la_get_device_status", "la_version", "la_launch_count"]:
+                 "la_status_string", "la_get_device_status", "la_version", "la_launch_count",
+                 "la_prefill_path"]:
         assert want in names
 
 
@@ -112,6 +113,14 @@ def test_decode_rejects_on_host(lib, args, want):
     rc = lib.la_decode_step_ex(a["state"], P[1], P[2], P[3], P[4], a["out"], None, a["B"],
                                a["H"], a["d"], a["dtype"], 1e-6, None)
     assert rc == want
+
+
+def test_prefill_path_rejects_on_host(lib):
+    assert lib.la_prefill_path(0, 1, 1, 128, la.LA_BF16, 0) == -la.LA_ERR_INVALID_ARG
+    assert lib.la_prefill_path(1, 1, 1, 64, la.LA_BF16, 0) == -la.LA_ERR_UNSUPPORTED
+    assert lib.la_prefill_path(1, 1, 1, 128, 9, 0) == -la.LA_ERR_INVALID_ARG
+    assert lib.la_prefill_path(1, 1, 1, 128, la.LA_F32, 0) == 1   # fp32: CUDA-core kernel
+    assert lib.la_prefill_path(1, 1, 1, 128, la.LA_BF16, la.LA_FLAG_SIMT) == 1
 
 
 def test_decode_entry_rejects_on_host(lib):

@@ -62,7 +62,10 @@ def test_prefill_state_equals_decode_steps(env, simt):
                               v[:, t].contiguous(), g[:, t].contiguous())
         assert rel_max_err(host64(o), host64(out[:, t])) <= 1e-2
     torch.cuda.synchronize()
-    assert rel_max_err(host64(Sd), host64(S)) <= 1e-5
+    # the tensor-core prefill forms k^T v from bf16-rounded operands; the decode kernel
+    # and the CUDA-core prefill stay in fp32
+    tol = 1e-5 if simt else TOL["bf16"]["state"]
+    assert rel_max_err(host64(Sd), host64(S)) <= tol
 
 
 def test_decode_b256_workload(env):

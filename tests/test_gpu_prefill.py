@@ -9,7 +9,7 @@ determinism, guard bands).
 import numpy as np
 import pytest
 
-from parity_util import TOL, host64, rel_max_err, row_rel_err
+from parity_util import TOL, elem_bound_ok, host64, rel_max_err, row_rel_err, y_abs_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -46,13 +46,27 @@ def _check_prefill(env, B, N, H, dt, scale, seed, simt, S0=False):
                                         S0=None if S_in is None else host64(S_in))
     tol = TOL[dt]
     e_out = rel_max_err(host64(out), ref_out)
-    e_y = row_rel_err(host64(y), ref_y)
+    e_y = row_rel_err(host64(y), ref_y, axes=(-2, -1))
     e_S = rel_max_err(host64(S), ref_S)
+    yabs = y_abs_bound(orc, host64(q), host64(k), host64(v),
+                       None if S_in is None else host64(S_in))
+    ok_elem, worst = elem_bound_ok(host64(y), ref_y, yabs, tol["y_elem"])
     assert e_out <= tol["out"], f"out rel err {e_out:.3e}"
-    assert e_y <= tol["y_row"], f"y row err {e_y:.3e}"
+    assert e_y <= tol["y_row"], f"y token-row err {e_y:.3e}"
+    assert ok_elem, f"y exceeds the elementwise bound by x{worst:.2f}"
     assert e_S <= tol["state"], f"state rel err {e_S:.3e}"
     assert np.isfinite(host64(out)).all()
     return e_out, e_y, e_S
+
+
+def test_tensor_core_path_selected(env):
+    """bf16 at the 64-head shapes runs the tensor-core kernel; fp32 or the flag the
+    CUDA-core one."""
+    torch, la, _ = env
+    for N in (1, 300, 8192, 131072, 1 << 20):
+        assert la.la_prefill_path(1, 64, N) == 0, N
+    assert la.la_prefill_path(1, 64, 8192, simt=True) == 1
+    assert la.la_prefill_path(1, 64, 8192, dtype=la.LA_F32) == 1
 
 
 def test_tiny_f32_workload(env):
