@@ -21,12 +21,9 @@ is needed between steps.  Printed as one JSON line:
 from __future__ import annotations
 
 import argparse
-import csv
 import hashlib
-import io
 import json
 import os
-import subprocess
 import sys
 import time
 
@@ -42,7 +39,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="prefill_8k")
@@ -96,49 +93,114 @@ def barrier():
         dist.barrier()
 
 
+class _Nvml:
+    """The few NVML queries the clock sampler needs: pynvml when installed, else the
+    driver's libnvidia-ml through ctypes (read-only queries)."""
+    SM = 1  # NVML_CLOCK_SM
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+            "hw_thermal_slowdown": 0x40, "hw_power_brake": 0x80}
+
+    def __init__(self, index: int):
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.py = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            return
+        except Exception:  # noqa: BLE001 - fall back to the C library
+            self.py = None
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index),
+                                                  ctypes.byref(self.h)) != 0:
+            raise RuntimeError("nvmlDeviceGetHandleByIndex_v2 failed")
+        self.reason_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sm_clock(self) -> int:
+        if self.py:
+            return self.py.nvmlDeviceGetClockInfo(self.h, self.SM)
+        v = self.c.c_uint()
+        self.lib.nvmlDeviceGetClockInfo(self.h, self.SM, self.c.byref(v))
+        return v.value
+
+    def max_clock(self) -> int:
+        if self.py:
+            return self.py.nvmlDeviceGetMaxClockInfo(self.h, self.SM)
+        v = self.c.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.SM, self.c.byref(v))
+        return v.value
+
+    def reasons(self) -> int:
+        if self.py:
+            return self.py.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+        v = self.c.c_ulonglong()
+        self.reason_fn(self.h, self.c.byref(v))
+        return v.value
+
+
 class ClockSampler:
-    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """Samples the SM clock and the clock-event (throttle) reasons through NVML from a
+    background thread while the timed region runs (every ~2 ms; the GIL is free while
+    the host waits on the GPU)."""
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
-        self.proc = None
+        self.thread = None
+        self.samples = []
+        self.reasons = set()
+        self.err = None
 
     def start(self):
+        import threading
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+            idx = self.gpu
+            if vis:
+                first = vis.split(",")[self.gpu].strip()
+                idx = int(first) if first.isdigit() else self.gpu
+            self.nv = _Nvml(idx)
+            self.max_mhz = self.nv.max_clock()
+        except Exception as e:  # noqa: BLE001 - reported in the JSON line
+            self.err = f"nvml unavailable: {e}"
+            return
+        self.stop_evt = threading.Event()
+        self.first = threading.Event()
+
+        def loop():
+            while not self.stop_evt.is_set():
+                try:
+                    self.samples.append(self.nv.sm_clock())
+                    bits = self.nv.reasons()
+                    for name, bit in _Nvml.BITS.items():
+                        if bits & bit:
+                            self.reasons.add(name)
+                except Exception as e:  # noqa: BLE001
+                    self.err = str(e)
+                    break
+                self.first.set()
+                time.sleep(0.002)
+            self.first.set()
+
+        self.thread = threading.Thread(target=loop, daemon=True)
+        self.thread.start()
+        self.first.wait(2.0)
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
-        sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            try:
-                sm.append(float(r[1]))
-                smax = float(r[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, r[5:9]):
-                if v.strip().lower() == "active":
-                    reasons.add(n)
-        sm.sort()
-        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        if self.thread is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": self.err}
+        self.stop_evt.set()
+        self.thread.join(2.0)
+        sm = sorted(self.samples)
+        d = {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": self.max_mhz,
+             "reasons": sorted(self.reasons), "samples": len(sm), "source": "nvml"}
+        if self.err:
+            d["error"] = self.err
+        return d
 
 
 def kernel_traffic(kernel: str, source_files):
