@@ -48,7 +48,8 @@ typedef enum {
     LA_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned                       */
     LA_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed            */
     LA_ERR_NOMEM = 5,       /* the workspace could not be grown                       */
-    LA_ERR_TIMEOUT = 6      /* a kernel gave up a bounded cross-CTA wait              */
+    LA_ERR_TIMEOUT = 6,     /* a kernel gave up a bounded cross-CTA wait              */
+    LA_ERR_SCRATCH_LIMIT = 7 /* B*H above LA_NOALLOC_MAX_HEADS (la_decode_step_noalloc) */
 } la_status;
 
 typedef enum {
@@ -110,6 +111,32 @@ int la_decode_step_ex(float* kv_state, const void* q, const void* k, const void*
    number of two-CTA clusters the device holds at once (it keeps every head of a
    token resident for the cross-head RMSNorm). */
 int la_prefill_path(int B, int H, int64_t N, int d, int dtype, unsigned flags);
+
+/*
+ * Decode step that allocates nothing.  The paper has no counterpart: this entry point
+ * exists for callers that cannot let a library call cudaMalloc -- for example a
+ * serving engine that has reserved all device memory for its own pool, or a
+ * latency-critical loop that cannot take the device synchronisation of
+ * cudaMalloc/cudaFree.  It computes exactly what la_decode_step_ex computes (same
+ * kernels, y_debug not offered), with the kernels' scratch (fp32 pre-norm y and
+ * per-head sums of squares) in a fixed array inside the library's device data:
+ *   - the array holds LA_NOALLOC_MAX_HEADS * (d + 1) floats (8.06 MiB), and every GPU
+ *     that loads the library keeps it until the process exits;
+ *   - B * H above LA_NOALLOC_MAX_HEADS returns LA_ERR_SCRATCH_LIMIT before any launch;
+ *   - the first call on a device looks the array's device address up (one
+ *     cudaGetSymbolAddress with that device current) and caches it; make that first
+ *     call before any stream capture on that device;
+ *   - all calls on a device share the one array and it keeps the last call's
+ *     contents: calls whose kernels may overlap on the GPU (different streams with
+ *     no ordering between them) race on it and must be ordered by the caller.
+ * The kernels write every scratch entry they read, so nothing is cleared between
+ * calls.  Arguments, layouts, dtype and eps are as for la_decode_step_ex; argument
+ * errors are returned before any launch.
+ */
+#define LA_NOALLOC_MAX_HEADS 16384 /* B * H, e.g. 256 sequences x 64 heads */
+int la_decode_step_noalloc(float* kv_state, const void* q, const void* k, const void* v,
+                           const void* g, void* out, int B, int H, int d, int dtype,
+                           float eps, void* cuda_stream);
 
 /* Static text for an la_status value. */
 const char* la_status_string(int status);

@@ -10,6 +10,8 @@ Functions carry the C names:
 
 * ``la_prefill(q, k, v, g, ...)``       -- prefill of ``[B, N, H, d]`` inputs
 * ``la_decode_step(kv_state, q, ...)``  -- one token per sequence, ``[B, H, d]`` inputs
+* ``la_decode_step_noalloc``           -- the same step with the library's fixed scratch,
+                                          for callers that cannot let it allocate
 * ``la_prefill_path``                  -- which prefill kernel serves a shape
 * ``la_status_string``, ``la_get_device_status``, ``la_version``, ``la_launch_count``
 """
@@ -18,12 +20,13 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["la_prefill", "la_decode_step", "la_status_string", "la_get_device_status",
+__all__ = ["la_prefill", "la_decode_step", "la_decode_step_noalloc", "la_status_string", "la_get_device_status",
            "la_version", "la_launch_count", "la_prefill_path", "LaError", "library_path",
            "load_library", "LA_BF16", "LA_F32", "LA_FLAG_SIMT"]
 
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_MISALIGNED = 0, 1, 2, 3
-LA_ERR_CUDA, LA_ERR_NOMEM, LA_ERR_TIMEOUT = 4, 5, 6
+LA_ERR_CUDA, LA_ERR_NOMEM, LA_ERR_TIMEOUT, LA_ERR_SCRATCH_LIMIT = 4, 5, 6, 7
+LA_NOALLOC_MAX_HEADS = 16384
 LA_BF16, LA_F32 = 0, 1
 LA_FLAG_SIMT = 1
 
@@ -62,6 +65,8 @@ def load_library():
     lib.la_decode_step.restype = i32
     lib.la_decode_step_ex.argtypes = [fp, vp, vp, vp, vp, vp, fp, i32, i32, i32, i32, f32, vp]
     lib.la_decode_step_ex.restype = i32
+    lib.la_decode_step_noalloc.argtypes = [fp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, vp]
+    lib.la_decode_step_noalloc.restype = i32
     lib.la_status_string.argtypes = [i32]
     lib.la_status_string.restype = ctypes.c_char_p
     lib.la_get_device_status.argtypes = [vp]
@@ -189,3 +194,29 @@ def la_decode_step(kv_state, q, k, v, g, out=None, y_debug=None, eps: float = 1e
     if rc != LA_OK:
         raise LaError(rc, "la_decode_step")
     return out
+
+
+def la_decode_step_noalloc(kv_state, q, k, v, g, out, eps: float = 1e-6, stream=None):
+    """``la_decode_step`` for callers that cannot let the library allocate device
+    memory: the kernels' scratch is a fixed array inside the library (up to
+    ``LA_NOALLOC_MAX_HEADS`` = B*H heads).  ``out`` must be given, so this wrapper
+    allocates nothing either.  Calls on one device share the scratch: order calls
+    that could overlap on the GPU."""
+    B, H, d = q.shape
+    _check([kv_state, q, k, v, g, out], ["kv_state", "q", "k", "v", "g", "out"])
+    for t, n in ((k, "k"), (v, "v"), (g, "g"), (out, "out")):
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{n} must match q in shape and dtype")
+    if tuple(kv_state.shape) != (B, H, d, d) or kv_state.dtype != _float32():
+        raise ValueError("kv_state must be float32 [B, H, d, d]")
+    rc = load_library().la_decode_step_noalloc(
+        _ptr(kv_state), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out), B, H, d,
+        _dtype_code(q), float(eps), _stream_handle(stream))
+    if rc != LA_OK:
+        raise LaError(rc, "la_decode_step_noalloc")
+    return out
+
+
+def _float32():
+    import torch
+    return torch.float32

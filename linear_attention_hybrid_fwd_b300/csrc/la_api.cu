@@ -85,6 +85,8 @@ const char* la_status_string(int s) {
         case LA_ERR_CUDA: return "CUDA error";
         case LA_ERR_NOMEM: return "out of device memory for the workspace";
         case LA_ERR_TIMEOUT: return "a kernel gave up a bounded cross-CTA wait";
+        case LA_ERR_SCRATCH_LIMIT:
+            return "B*H exceeds the fixed scratch of la_decode_step_noalloc";
         default: return "unknown status";
     }
 }
