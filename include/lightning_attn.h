@@ -107,9 +107,10 @@ int la_decode_step_ex(float* kv_state, const void* q, const void* k, const void*
 
 /* Which prefill kernel la_prefill_ex would run for this shape on the current device:
    0 = tensor-core kernel, 1 = CUDA-core kernel, or -(la_status) if the arguments are
-   invalid.  The tensor-core kernel covers bf16, d = 128, and B*H no larger than the
-   number of two-CTA clusters the device holds at once (it keeps every head of a
-   token resident for the cross-head RMSNorm). */
+   invalid.  The tensor-core kernel covers bf16, d = 128, H no larger than the number
+   of two-CTA clusters the device holds at once (it keeps every head resident for the
+   cross-head RMSNorm and runs the B sequences one after another), N <= 2^30 and
+   B * ceil(N / 128) <= 131072. */
 int la_prefill_path(int B, int H, int64_t N, int d, int dtype, unsigned flags);
 
 /*
@@ -118,10 +119,11 @@ int la_prefill_path(int B, int H, int64_t N, int d, int dtype, unsigned flags);
  * serving engine that has reserved all device memory for its own pool, or a
  * latency-critical loop that cannot take the device synchronisation of
  * cudaMalloc/cudaFree.  It computes exactly what la_decode_step_ex computes (same
- * kernels, y_debug not offered), with the kernels' scratch (fp32 pre-norm y and
- * per-head sums of squares) in a fixed array inside the library's device data:
- *   - the array holds LA_NOALLOC_MAX_HEADS * (d + 1) floats (8.06 MiB), and every GPU
- *     that loads the library keeps it until the process exits;
+ * kernel, y_debug not offered), with the kernel's scratch (fp32 pre-norm y, per-head
+ * sums of squares and per-sequence arrival counters) in a fixed array inside the
+ * library's device data:
+ *   - the array holds LA_NOALLOC_MAX_HEADS * (d + 2) 4-byte words (8.13 MiB), and every
+ *     GPU that loads the library keeps it until the process exits;
  *   - B * H above LA_NOALLOC_MAX_HEADS returns LA_ERR_SCRATCH_LIMIT before any launch;
  *   - the first call on a device looks the array's device address up (one
  *     cudaGetSymbolAddress with that device current) and caches it; make that first
@@ -129,8 +131,8 @@ int la_prefill_path(int B, int H, int64_t N, int d, int dtype, unsigned flags);
  *   - all calls on a device share the one array and it keeps the last call's
  *     contents: calls whose kernels may overlap on the GPU (different streams with
  *     no ordering between them) race on it and must be ordered by the caller.
- * The kernels write every scratch entry they read, so nothing is cleared between
- * calls.  Arguments, layouts, dtype and eps are as for la_decode_step_ex; argument
+ * The kernel writes every scratch entry it reads and returns each counter it uses to
+ * zero, so nothing is cleared between calls.  Arguments, layouts, dtype and eps are as for la_decode_step_ex; argument
  * errors are returned before any launch.
  */
 #define LA_NOALLOC_MAX_HEADS 16384 /* B * H, e.g. 256 sequences x 64 heads */

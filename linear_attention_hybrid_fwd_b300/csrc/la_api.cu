@@ -26,6 +26,7 @@ struct WorkspaceReaper {
         for (auto& w : g_ws) {
             if (w.base) cudaFree(w.base);
             if (w.status) cudaFree(w.status);
+            if (w.banks) cudaFree(w.banks);
         }
     }
 } g_reaper;
@@ -44,14 +45,34 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; 
 
 void note_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
-int workspace_acquire(size_t bytes, Workspace* out) {
+int workspace_acquire(size_t bytes, cudaStream_t st, Workspace* out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_ws_mutex);
     Workspace& w = g_ws[dev];
     if (!w.status) {
-        if (cudaMalloc(&w.status, 256) != cudaSuccess) return LA_ERR_NOMEM;
-        if (cudaMemset(w.status, 0, 256) != cudaSuccess) return LA_ERR_CUDA;
+        int* status = nullptr;
+        unsigned* banks = nullptr;
+        if (cudaMalloc(&status, 256) != cudaSuccess) {
+            cudaGetLastError();
+            return LA_ERR_NOMEM;
+        }
+        const size_t cbytes = 2 * kTcCounterBytes + size_t(kDecodeCounterSlots) * sizeof(unsigned);
+        if (cudaMalloc(&banks, cbytes) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(status);
+            return LA_ERR_NOMEM;
+        }
+        if (cudaMemsetAsync(status, 0, 256, st) != cudaSuccess ||
+            cudaMemsetAsync(banks, 0, cbytes, st) != cudaSuccess) {
+            cudaFree(status);
+            cudaFree(banks);
+            return LA_ERR_CUDA;
+        }
+        w.status = status;
+        w.banks = banks;
+        w.dec_cnt = banks + 2 * kTcCounterSlots;
+        w.bank = 0;
     }
     if (bytes > w.bytes) {
         // cudaFree waits for work already queued on the device, so a smaller
@@ -68,6 +89,13 @@ int workspace_acquire(size_t bytes, Workspace* out) {
     }
     *out = w;
     return LA_OK;
+}
+
+void workspace_switch_bank() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return;
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    g_ws[dev].bank ^= 1u;
 }
 
 }  // namespace la
@@ -142,7 +170,7 @@ int la_prefill_ex(const void* q, const void* k, const void* v, const void* g, vo
     const bool use_tc = bf16 && !(flags & LA_FLAG_SIMT) && prefill_tc_supported(B, H, N) == LA_OK;
     if (use_tc) {
         Workspace ws;
-        int rc = workspace_acquire(prefill_tc_workspace_bytes(B, H, N), &ws);
+        int rc = workspace_acquire(prefill_tc_workspace_bytes(B, H, N), st, &ws);
         if (rc != LA_OK) return rc;
         return launch_prefill_tc(q, k, v, g, out, kv_state_in, kv_state_out, y_debug, B, H, N,
                                  eps, ws, st);
@@ -151,7 +179,7 @@ int la_prefill_ex(const void* q, const void* k, const void* v, const void* g, vo
     float* y = y_debug;
     if (!y) {
         Workspace ws;
-        int rc = workspace_acquire((size_t)nelem * sizeof(float), &ws);
+        int rc = workspace_acquire((size_t)nelem * sizeof(float), st, &ws);
         if (rc != LA_OK) return rc;
         y = static_cast<float*>(ws.base);
     }
@@ -200,13 +228,13 @@ int la_decode_step_ex(float* kv_state, const void* q, const void* k, const void*
     if (overlaps(kv_state, state_bytes, out, io_bytes)) return LA_ERR_INVALID_ARG;
 
     const size_t ny = (size_t)B * H * d;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
     Workspace ws;
-    int rc = workspace_acquire((ny + (size_t)B * H) * sizeof(float) + 256, &ws);
+    int rc = workspace_acquire((ny + (size_t)B * H) * sizeof(float) + 256, st, &ws);
     if (rc != LA_OK) return rc;
     float* y = y_debug ? y_debug : static_cast<float*>(ws.base);
     float* ss = static_cast<float*>(ws.base) + ny;
-    return launch_decode(kv_state, q, k, v, g, out, y, ss, B, H, eps, bf16,
-                         reinterpret_cast<cudaStream_t>(cuda_stream));
+    return launch_decode(kv_state, q, k, v, g, out, y, ss, ws.dec_cnt, B, H, eps, bf16, st);
 }
 
 int la_decode_step(float* kv_state, const void* q, const void* k, const void* v,
@@ -219,8 +247,9 @@ int la_get_device_status(void* cuda_stream) {
     cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
     if (cudaStreamSynchronize(st) != cudaSuccess) return LA_ERR_CUDA;
     Workspace ws;
-    int rc = workspace_acquire(0, &ws);
+    int rc = workspace_acquire(0, st, &ws);
     if (rc != LA_OK) return rc;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return LA_ERR_CUDA;
     int h = 0;
     if (cudaMemcpy(&h, ws.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
         return LA_ERR_CUDA;

@@ -1,16 +1,16 @@
 // la_noalloc.cu -- la_decode_step_noalloc: the decode step for callers that must not
 // allocate device memory.
 //
-// la_decode_step_ex keeps its fp32 pre-norm y and the per-head sums of squares in a
-// workspace it grows with cudaMalloc on first use.  Some callers cannot let a library
-// do that: a serving engine that has reserved all of HBM for its own pool (a stray
-// cudaMalloc would fail or eat into the pool), or a latency-critical loop where the
-// implicit device synchronisation of cudaMalloc/cudaFree is not acceptable.  This entry
-// point runs the same two decode kernels with their scratch taken from a fixed array
-// in the library's own device data instead.
+// la_decode_step_ex keeps its fp32 pre-norm y, the per-head sums of squares and the
+// per-sequence arrival counters in a workspace it allocates with cudaMalloc on first
+// use.  Some callers cannot let a library do that: a serving engine that has reserved
+// all of HBM for its own pool (a stray cudaMalloc would fail or eat into the pool), or
+// a latency-critical loop where the implicit device synchronisation of
+// cudaMalloc/cudaFree is not acceptable.  This entry point runs the same decode kernel
+// with its scratch taken from a fixed array in the library's own device data instead.
 //
-// The scratch is a file-scope __device__ array of kNoAllocScratchFloats floats
-// (8.06 MiB), which every device that loads this library holds until the process
+// The scratch is a file-scope __device__ array of kNoAllocScratchFloats 4-byte words
+// (8.13 MiB), which every device that loads this library holds until the process
 // exits.  Host code cannot use the array's name as a device address (on the host it
 // names a host-side shadow), so the first call on each device looks the address up
 // with cudaGetSymbolAddress while that device is current and caches it.
@@ -26,9 +26,11 @@
 namespace la {
 namespace {
 
-// y [B*H][d] fp32 followed by ss [B*H] fp32, for up to LA_NOALLOC_MAX_HEADS heads.
+// y [B*H][d] fp32, then ss [B*H] fp32, then one arrival counter per sequence (B <= B*H),
+// for up to LA_NOALLOC_MAX_HEADS heads.  The counters start at zero (static storage)
+// and every call leaves them at zero.
 constexpr size_t kNoAllocScratchFloats =
-    size_t(LA_NOALLOC_MAX_HEADS) * kHeadDim + size_t(LA_NOALLOC_MAX_HEADS);
+    size_t(LA_NOALLOC_MAX_HEADS) * kHeadDim + 2 * size_t(LA_NOALLOC_MAX_HEADS);
 
 __device__ __align__(256) float g_decode_scratch[kNoAllocScratchFloats];
 
@@ -90,10 +92,11 @@ extern "C" int la_decode_step_noalloc(float* kv_state, const void* q, const void
 
     float* scratch = scratch_on_current_device();
     if (!scratch) return LA_ERR_CUDA;
-    // Both kernels write every y and ss entry they later read, so the scratch needs no
-    // clearing between calls.
+    // The kernel writes every y and ss entry it later reads, and returns each counter it
+    // uses to zero, so the scratch needs no clearing between calls.
     float* y = scratch;
     float* ss = scratch + (size_t)LA_NOALLOC_MAX_HEADS * kHeadDim;
-    return launch_decode(kv_state, q, k, v, g, out, y, ss, B, H, eps, bf16,
+    unsigned* cnt = reinterpret_cast<unsigned*>(ss + LA_NOALLOC_MAX_HEADS);
+    return launch_decode(kv_state, q, k, v, g, out, y, ss, cnt, B, H, eps, bf16,
                          reinterpret_cast<cudaStream_t>(cuda_stream));
 }

@@ -6,29 +6,39 @@
 // product takes the blockwise O(d^2 n) route of the same section: per chunk c of 128
 // tokens
 //     Y_c = Q^_c S_{<c} + (Q^_c K^_c^T * M) V^_c ,    S_{<c+1} = S_{<c} + K^_c^T V^_c
-// with M the inclusive lower-triangular mask.
+// with M the inclusive lower-triangular mask and S the fp32 d x d state.
 //
-// Design (one B300 SM per CTA, 224 KiB shared memory, all 512 TMEM columns):
-//  * A cluster of two CTAs owns one (sequence b, head h).  CTA r takes the chunks
-//    c = r, r+2, r+4, ... and keeps the partial state S_r = sum of K^T V over ITS
-//    chunks in TMEM (fp32).  S_{<c} = S_0 + S_1 is applied as two MMAs, Q^ S_own and
-//    Q^ S_peer; after each chunk a CTA converts its S_own to bf16 and bulk-copies it
-//    into the peer's shared memory.  Only a d x d state crosses the pair, and the
-//    pair has no redundant loads or activations.
-//  * Warp roles: warp 0 issues TMA loads (q, k, v tiles, 128B-swizzled), warp 1 issues
-//    tcgen05 MMAs, warp 2 owns TMEM, warps 4-7 apply SiLU (q into TMEM as the A
-//    operand; k, v in place in shared memory), mask the score tile and convert the
-//    state, warps 8-15 run the epilogue.
-//  * The RMSNorm spans all heads of a token, so the epilogue exchanges per-token
-//    partial sums of squares through global memory: every head's CTA for chunk c
-//    writes its 128 partials, bumps a counter and waits (bounded) until all H have
-//    arrived, then sums the H partials in a fixed order (deterministic).  All CTAs of
-//    the grid must be co-resident; the host checks that before launching.
+// Design (one B300 SM per CTA, 212 KiB shared memory, all 512 TMEM columns):
+//  * A cluster of two CTAs owns one head h and runs through every chunk of every
+//    sequence of the batch in order.  The pair splits the d_v columns: CTA r keeps the
+//    state columns S[:, 64r, 64r+64) in TMEM and produces y and out for those columns.
+//    Nothing on the state's chunk-to-chunk path crosses the pair.
+//  * The activations are not duplicated: CTA 0 loads q and applies SiLU, CTA 1 does the
+//    same for k, and each bulk-copies its activated 128 x 128 tile into the other's
+//    shared memory.  Each CTA activates its own 64 columns of v.  Both then form the
+//    full score tile Q^ K^T (an MMA, cheap) and their halves of the products.
+//  * Warp roles (28 warps): warp 0 issues TMA loads, warp 1 issues tcgen05 MMAs, warp 2
+//    owns TMEM; warps 4-11 apply SiLU in shared memory and push the activated tile to
+//    the peer; warps 12-15 convert the fp32 state to the bf16 operand of Q^ S and mask
+//    the score tile into the bf16 P operand (written in place over the scores);
+//    warps 16-19 post each chunk's per-token sums of squares; warps 20-23 and 24-27
+//    take alternate chunks and finish them (norm, gate, store).
+//  * The RMSNorm spans all heads of a token.  Per chunk, CTA 1 hands its per-token sums
+//    of squares to CTA 0 through distributed shared memory; CTA 0 writes the head's
+//    sums to a global exchange slot and bumps the slot's counter; a finishing
+//    warpgroup waits (bounded) for all H heads and sums them in a fixed order
+//    (deterministic).  y stays in TMEM (three buffers) while the exchange is in flight,
+//    so its latency is not on the per-chunk path.  All CTAs of the grid must be
+//    co-resident; the host checks that before launching.
+//  * Out tiles leave by TMA store from swizzled staging tiles; q, k, v arrive by TMA in
+//    128B-swizzled tiles, double-buffered.  The score tile is double-buffered in TMEM.
+//  * SiLU(x) = x/2 (1 + tanh(x/2)) and sigmoid(x) = (1 + tanh(x/2))/2 with the hardware
+//    tanh approximation: one SFU operation per element.
 //  * Every wait is bounded (%globaltimer); a CTA that gives up records LA_ERR_TIMEOUT
 //    in the status word, drains its in-flight copies and MMAs, frees TMEM and exits.
 //
-// TMEM columns: [0,128) S_own fp32 | [128,256) scores A fp32 | [256,384) Y fp32 |
-//               [384,448) Q^ bf16x2 (A operand) | [448,512) P = mask(A) bf16x2.
+// TMEM columns: [0,128) scores A0 (P0 over its first 64) | [128,256) A1 (P1) |
+//               [256,320) S (fp32, this CTA's 64 columns) | [320,512) Y0, Y1, Y2.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -48,58 +58,79 @@ using namespace sm100;
 
 constexpr int D = kHeadDim;
 constexpr int CH = 128;               // tokens per chunk
-constexpr int kThreads = 512;
+constexpr int DV = 64;                // d_v columns per CTA
+constexpr int kThreads = 896;         // 28 warps
+constexpr int kYBufs = 3;
+// CTA 1 posts chunk it only after CTA 0 posted chunk it - kYBufs (through the y ring and
+// the exchange), so kYBufs slots of the pair hand-off never alias.
+constexpr int kPairSlots = kYBufs;
+constexpr int kGBufs = 2;             // g tiles in flight (TMA-loaded ahead of the epilogue)
 constexpr uint32_t TILE = 32768;      // 128 x 128 bf16 = two swizzled 128 x 64 halves
-constexpr uint32_t HALF = 16384;
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = OFF_Q + TILE;        // two stages
-constexpr uint32_t OFF_V = OFF_K + 2 * TILE;    // two stages
-constexpr uint32_t OFF_SOWN = OFF_V + 2 * TILE;
-constexpr uint32_t OFF_SPEER = OFF_SOWN + TILE;
-constexpr uint32_t SMEM_USED = OFF_SPEER + TILE;  // 224 KiB
-constexpr uint32_t SMEM_DYN = SMEM_USED + 1024;   // + alignment slack
-constexpr uint32_t TM_S = 0, TM_A = 128, TM_Y = 256, TM_Q = 384, TM_P = 448;
-constexpr uint64_t kTimeoutNs = 4000000000ull;    // 4 s
-constexpr uint64_t kDrainNs = 200000000ull;       // 0.2 s
+constexpr uint32_t HALF = 16384;      // 128 x 64 bf16, one 128B-swizzled block
+constexpr uint32_t OFF_QB = 0;                  // 2 stages: q^ tiles
+constexpr uint32_t OFF_KB = OFF_QB + 2 * TILE;  // 2 stages: k^ tiles
+constexpr uint32_t OFF_VB = OFF_KB + 2 * TILE;  // 2 stages: v^ (this CTA's 64 columns)
+constexpr uint32_t OFF_SB = OFF_VB + 2 * HALF;  // bf16 state slice (MN-major B operand)
+constexpr uint32_t OFF_GB = OFF_SB + HALF;      // kGBufs g tiles (this CTA's 64 columns)
+constexpr uint32_t SMEM_USED = OFF_GB + kGBufs * HALF;  // 208 KiB
+constexpr uint32_t SMEM_DYN = SMEM_USED + 1024; // + alignment slack
+static_assert(SMEM_DYN + sizeof(uint64_t) * 64 + 4096 <= 227 * 1024, "shared memory budget");
+constexpr uint32_t TM_A = 0, TM_S = 256, TM_Y = 320;
+constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s
+constexpr uint64_t kDrainNs = 200000000ull;     // 0.2 s
 
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, 0, 0);  // A K-major, B K-major
-constexpr uint32_t IDESC_XB = idesc_bf16_f32(128, 128, 0, 1);  // A K-major, B MN-major
-constexpr uint32_t IDESC_KV = idesc_bf16_f32(128, 128, 1, 1);  // A MN-major, B MN-major
+constexpr uint32_t IDESC_QS = idesc_bf16_f32(128, DV, 0, 1);   // A K-major, B MN-major
+constexpr uint32_t IDESC_KV = idesc_bf16_f32(128, DV, 1, 1);   // A MN-major, B MN-major
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, DV, 0, 1);   // A (TMEM), B MN-major
 
 struct Params {
-    const __nv_bfloat16* g;
     __nv_bfloat16* out;
     const float* S_in;
     float* S_out;
     float* y_dbg;
-    float* xch;      // [B][Nc][128][H] per-token, per-head partial sums of squares
-    unsigned* cnt;   // [B][Nc] arrival counters (zeroed before launch)
+    float* xch;          // [B*Nc][CH][H] per-token, per-head sums of squares
+    unsigned* cnt;       // [B*Nc] arrivals of this launch (zero on entry)
+    unsigned* cnt_clear; // the other counter bank, zeroed for the next launch
+    int n_clear;
     int* status;
     int B, H;
     int64_t N;
     int Nc;
     float eps;
-    float inv_width;  // 1 / (H * d)
+    float inv_width;     // 1 / (H * d)
 };
 
 struct Shared {
-    uint64_t qfull, qempty, kvfull[2], kvready[2], kvempty[2], qhfull, qhempty, afull, pfull,
-        sdone, sownfull, speerfull, peercons, yfull, yempty, mmadone;
+    uint64_t rawfull[2], xin[2], actdone[2], empty[2];
+    uint64_t afull[2], aempty[2], pfull, sdone, sready;
+    uint64_t yfull[kYBufs], yempty[kYBufs], gfull[kGBufs], gempty[kGBufs];
+    uint64_t ssown[kPairSlots], ssx[kPairSlots], mmadone;
     uint32_t tmem_base;
     int abort_flag;
-    int verdict[2];   // group-uniform wait results (WG1, WG2)
-    float red[2][CH];
-    float rnorm[CH];
+    int verdict[5];  // group-uniform wait results (SiLU, mask, post, finish 0, finish 1)
+    int issued;      // iterations whose loads the producer issued
+    int xin_seen;    // iterations whose peer tile the MMA issuer consumed
+    int g_issued;    // iterations whose g tile was issued
+    float own[kPairSlots][CH];  // this CTA's per-token sums of squares (CTA 0 only)
+    float xs[kPairSlots][CH];   // CTA 1's per-token sums of squares (received by CTA 0)
 };
 
 // ------------------------------------------------------------------ numerics
-// sigmoid(x) = 1 / (1 + e^-x) and SiLU(x) = x sigmoid(x), with the fast CUDA
-// intrinsics (relative error ~1e-6 over the input range; the bf16 rounding of the
-// result, 2^-9, dominates).
-__device__ __forceinline__ float sigmoid_fast(float x) {
-    return __fdividef(1.0f, 1.0f + __expf(-x));
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
-__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+// SiLU(x) = x sigmoid(x) = h (1 + tanh(h)) with h = x/2.
+__device__ __forceinline__ float silu_t(float x) {
+    const float h = 0.5f * x;
+    return fmaf(h, tanh_approx(h), h);
+}
+// sigmoid(x) = (1 + tanh(x/2)) / 2.
+__device__ __forceinline__ float sigmoid_t(float x) {
+    return fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
@@ -109,15 +140,25 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 __device__ __forceinline__ uint32_t silu_bf16x2(uint32_t u) {
-    return pack_bf16x2(silu_fast(bf_lo(u)), silu_fast(bf_hi(u)));
+    return pack_bf16x2(silu_t(bf_lo(u)), silu_t(bf_hi(u)));
 }
 __device__ __forceinline__ uint4 silu_chunk(uint4 v) {
     return make_uint4(silu_bf16x2(v.x), silu_bf16x2(v.y), silu_bf16x2(v.z), silu_bf16x2(v.w));
 }
 
-// Byte offset of the 16-byte chunk `c` (0..7) of row `r` in a 128B-swizzled half tile.
+// Byte offset of the 16-byte chunk `c` (0..7) of row `r` in a 128B-swizzled block.
 __device__ __forceinline__ uint32_t swz(int r, int c) {
     return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// Smem descriptors.  K-major operand with K = 128 split into two 64-wide swizzled
+// halves; k-step ks (16 elements = 32 bytes).  MN-major operand: k-step ks covers 16 rows
+// (2048 bytes); `lbo` is the distance between 64-element MN blocks.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int ks) {
+    return smem_desc_sw128(base + (ks >> 2) * HALF + (ks & 3) * 32, 16, 1024);
+}
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int ks) {
+    return smem_desc_sw128(base + ks * 2048, HALF, 1024);
 }
 
 // ------------------------------------------------------------------ bounded waits
@@ -130,12 +171,16 @@ __device__ __forceinline__ void raise_abort(Shared& sh, int* status) {
 }
 // Waits for the phase of `bar` with `parity` to complete.  Gives up (false) when the
 // CTA is aborting (honor_abort) or after `limit_ns`, raising the abort itself.
+template <bool kCluster = false>
 __device__ bool wait_bar(Shared& sh, int* status, uint64_t* bar, uint32_t parity,
                          bool honor_abort = true, uint64_t limit_ns = kTimeoutNs) {
-    if (mbar_try_wait(bar, parity)) return true;
-    uint64_t t0 = global_timer_ns();
+    auto probe = [&]() {
+        return kCluster ? mbar_try_wait_acq_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    };
+    if (probe()) return true;
+    const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (probe()) return true;
         if ((it & 15u) == 0) {
             if (honor_abort && abort_set(sh)) return false;
             if (global_timer_ns() - t0 > limit_ns) {
@@ -146,24 +191,32 @@ __device__ bool wait_bar(Shared& sh, int* status, uint64_t* bar, uint32_t parity
     }
 }
 // Group-uniform wait: thread `leader` waits (bounded), the group of `n` threads syncs on
-// named barrier `id`, then every thread observes the completed phase itself.
+// named barrier `id`, then every thread observes the completed phase itself.  No
+// barrier used with it can complete a further phase before every thread of the group
+// has observed this one (each next phase needs an arrival from this group).
+template <bool kCluster = false>
 __device__ bool group_wait(Shared& sh, int* status, uint64_t* bar, uint32_t parity, bool leader,
                            uint32_t id, uint32_t n, int slot) {
-    if (leader) sh.verdict[slot] = wait_bar(sh, status, bar, parity) ? 1 : 0;
+    if (leader) sh.verdict[slot] = wait_bar<kCluster>(sh, status, bar, parity) ? 1 : 0;
     named_bar_sync(id, n);
     const bool ok = *reinterpret_cast<volatile int*>(&sh.verdict[slot]) != 0;
-    if (ok)
-        while (!mbar_try_wait(bar, parity)) {
+    if (ok) {
+        if (kCluster) {
+            while (!mbar_try_wait_acq_cluster(bar, parity)) {
+            }
+        } else {
+            while (!mbar_try_wait(bar, parity)) {
+            }
         }
+    }
     named_bar_sync(id, n);  // verdict slot may be rewritten only after everyone read it
     return ok;
 }
 
-// Write 32 fp32 values (columns 32*part .. +31 of row r) as bf16 into an MN-major
-// 128B-swizzled 128 x 128 tile (two 128-column halves of 64).
-__device__ __forceinline__ void store_row_bf16(uint8_t* tile, int r, int part,
+// Write 32 fp32 values (columns 32*part .. +31 of row r, part 0 or 1) as bf16 into a
+// 128B-swizzled 128 x 64 block.
+__device__ __forceinline__ void store_row_bf16(uint8_t* blk, int r, int part,
                                                const uint32_t (&v)[32]) {
-    uint8_t* half = tile + (part >> 1) * HALF;
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc) {
         uint4 w;
@@ -171,14 +224,33 @@ __device__ __forceinline__ void store_row_bf16(uint8_t* tile, int r, int part,
         w.y = pack_bf16x2(__uint_as_float(v[8 * cc + 2]), __uint_as_float(v[8 * cc + 3]));
         w.z = pack_bf16x2(__uint_as_float(v[8 * cc + 4]), __uint_as_float(v[8 * cc + 5]));
         w.w = pack_bf16x2(__uint_as_float(v[8 * cc + 6]), __uint_as_float(v[8 * cc + 7]));
-        *reinterpret_cast<uint4*>(half + swz(r, (part & 1) * 4 + cc)) = w;
+        *reinterpret_cast<uint4*>(blk + swz(r, part * 4 + cc)) = w;
     }
 }
 
 // ------------------------------------------------------------------ the kernel
+// Bounded spin until *cnt >= target; false (after raising the abort) on timeout or when
+// the CTA is aborting.
+__device__ bool spin_counter(Shared& sh, int* status, const unsigned* cnt, unsigned target) {
+    uint64_t t0 = 0;
+    for (uint32_t k = 0;; ++k) {
+        if (ld_acquire_gpu(cnt) >= target) return true;
+        if ((k & 63u) == 63u) {
+            if (abort_set(sh)) return false;
+            const uint64_t now = global_timer_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > kTimeoutNs) {
+                raise_abort(sh, status);
+                return false;
+            }
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     k_prefill_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                 const __grid_constant__ CUtensorMap tv, const Params p) {
+                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
+                 const Params p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ Shared sh;
     uint8_t* sm = reinterpret_cast<uint8_t*>(
@@ -187,369 +259,373 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();
     const uint32_t peer = rank ^ 1u;
-    const int item = blockIdx.x >> 1;  // b * H + h
-    const int b = item / p.H, h = item % p.H;
-    const int Nc = p.Nc;
-    const int n_own = (Nc - static_cast<int>(rank) + 1) / 2;
-    const int n_peer = (Nc - static_cast<int>(peer) + 1) / 2;
+    const int h = blockIdx.x >> 1;
+    const int H = p.H, Nc = p.Nc;
+    const int total = p.B * Nc;                              // (sequence, chunk) iterations
+    const int col0 = h * D + static_cast<int>(rank) * DV;    // first feature column owned
+    const uint32_t own_off = rank == 0 ? OFF_QB : OFF_KB;    // the tile this CTA activates
+
+    // the other counter bank is zeroed here for the next launch
+    for (int i = blockIdx.x * kThreads + tid; i < p.n_clear; i += gridDim.x * kThreads)
+        p.cnt_clear[i] = 0u;
 
     if (tid == 0) {
-        mbar_init(&sh.qfull, 1);
-        mbar_init(&sh.qempty, 1);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&sh.kvfull[s], 1);
-            mbar_init(&sh.kvready[s], 1);
-            mbar_init(&sh.kvempty[s], 1);
+            mbar_init(&sh.rawfull[s], 1);
+            mbar_init(&sh.xin[s], 1);
+            mbar_init(&sh.actdone[s], 1);
+            mbar_init(&sh.empty[s], 2);  // this CTA's MMAs and the peer's
+            mbar_init(&sh.afull[s], 1);
+            mbar_init(&sh.aempty[s], 1);
         }
-        mbar_init(&sh.qhfull, 1);
-        mbar_init(&sh.qhempty, 1);
-        mbar_init(&sh.afull, 1);
+        for (int y = 0; y < kYBufs; ++y) {
+            mbar_init(&sh.yfull[y], 1);
+            mbar_init(&sh.yempty[y], 1);
+        }
+        for (int i = 0; i < kGBufs; ++i) {
+            mbar_init(&sh.gfull[i], 1);
+            mbar_init(&sh.gempty[i], 1);
+        }
+        for (int i = 0; i < kPairSlots; ++i) {
+            mbar_init(&sh.ssown[i], CH);  // this CTA's post warps, one arrival per row
+            mbar_init(&sh.ssx[i], CH);    // one remote arrival per token row of CTA 1
+        }
         mbar_init(&sh.pfull, 1);
         mbar_init(&sh.sdone, 1);
-        mbar_init(&sh.sownfull, 1);
-        mbar_init(&sh.speerfull, 1);
-        mbar_init(&sh.peercons, 1);
-        mbar_init(&sh.yfull, 1);
-        mbar_init(&sh.yempty, 1);
+        mbar_init(&sh.sready, 1);
         mbar_init(&sh.mmadone, 1);
         sh.abort_flag = 0;
-        sh.verdict[0] = sh.verdict[1] = 0;
+        for (int i = 0; i < 5; ++i) sh.verdict[i] = 0;
+        sh.issued = 0;
+        sh.xin_seen = 0;
+        sh.g_issued = 0;
         fence_mbar_init();
-        // the first bf16 state from the peer lands here; armed before the peer can send
-        if (n_own > 0) mbar_arrive_expect_tx(&sh.speerfull, TILE);
     }
     if (warp == 2) tmem_alloc(&sh.tmem_base, 512);
     tc_fence_before();
     __syncthreads();
-    cluster_sync();
+    cluster_sync();  // the peer's barriers are initialised before anything reaches them
     tc_fence_after();
     const uint32_t tm = sh.tmem_base;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer
         if (lane == 0) {
+            // -------------------------------------------- TMA producer: q or k, and v
+            const CUtensorMap* own_map = rank == 0 ? &tq : &tk;
             int issued = 0;
-            for (int i = 0; i < n_own; ++i) {
-                const int c = 2 * i + static_cast<int>(rank);
-                const int row0 = c * CH;
-                const int s = i & 1;
-                const uint32_t u = static_cast<uint32_t>(i >> 1);
-                if (!wait_bar(sh, p.status, &sh.kvempty[s], (u & 1u) ^ 1u)) break;
-                mbar_arrive_expect_tx(&sh.kvfull[s], 2 * TILE);
-                uint8_t* kt = sm + OFF_K + s * TILE;
-                uint8_t* vt = sm + OFF_V + s * TILE;
-                tma_load_3d(kt, &tk, h * D, row0, b, &sh.kvfull[s]);
-                tma_load_3d(kt + HALF, &tk, h * D + 64, row0, b, &sh.kvfull[s]);
-                tma_load_3d(vt, &tv, h * D, row0, b, &sh.kvfull[s]);
-                tma_load_3d(vt + HALF, &tv, h * D + 64, row0, b, &sh.kvfull[s]);
-                issued = i + 1;
-                if (!wait_bar(sh, p.status, &sh.qempty, static_cast<uint32_t>(i & 1) ^ 1u)) {
-                    issued = -issued;  // the q tile of this index was not issued
-                    break;
-                }
-                mbar_arrive_expect_tx(&sh.qfull, TILE);
-                tma_load_3d(sm + OFF_Q, &tq, h * D, row0, b, &sh.qfull);
-                tma_load_3d(sm + OFF_Q + HALF, &tq, h * D + 64, row0, b, &sh.qfull);
+            for (int it = 0; it < total; ++it) {
+                const int b = it / Nc, c = it - b * Nc;
+                const int s = it & 1;
+                const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
+                if (!wait_bar(sh, p.status, &sh.empty[s], ph ^ 1u)) break;
+                uint8_t* own = sm + own_off + s * TILE;
+                uint8_t* vt = sm + OFF_VB + s * HALF;
+                mbar_arrive_expect_tx(&sh.rawfull[s], TILE + HALF);
+                tma_load_3d(own, own_map, h * D, c * CH, b, &sh.rawfull[s]);
+                tma_load_3d(own + HALF, own_map, h * D + 64, c * CH, b, &sh.rawfull[s]);
+                tma_load_3d(vt, &tv, col0, c * CH, b, &sh.rawfull[s]);
+                mbar_arrive_expect_tx(&sh.xin[s], TILE);  // the peer's activated tile
+                issued = it + 1;
             }
-            // drain: every issued copy lands before this CTA may exit
-            const bool q_last_missing = issued < 0;
-            const int n_kv = issued < 0 ? -issued : issued;
-            for (int i = n_kv - 2 < 0 ? 0 : n_kv - 2; i < n_kv; ++i)
-                wait_bar(sh, p.status, &sh.kvfull[i & 1], static_cast<uint32_t>(i >> 1) & 1u,
-                         false, kDrainNs);
-            const int n_q = q_last_missing ? n_kv - 1 : n_kv;
-            if (n_q > 0)
-                wait_bar(sh, p.status, &sh.qfull, static_cast<uint32_t>(n_q - 1) & 1u, false,
-                         kDrainNs);
+            sh.issued = issued;
+            // drain: the last loads land before this CTA may exit
+            for (int it = issued - 2 < 0 ? 0 : issued - 2; it < issued; ++it)
+                wait_bar(sh, p.status, &sh.rawfull[it & 1],
+                         static_cast<uint32_t>(it >> 1) & 1u, false, kDrainNs);
+        } else if (lane == 1) {
+            // -------------------------------------------- TMA producer: g
+            int issued = 0;
+            for (int it = 0; it < total; ++it) {
+                const int b = it / Nc, c = it - b * Nc;
+                const int gs = it % kGBufs;
+                const uint32_t gph = static_cast<uint32_t>(it / kGBufs) & 1u;
+                if (!wait_bar(sh, p.status, &sh.gempty[gs], gph ^ 1u)) break;
+                mbar_arrive_expect_tx(&sh.gfull[gs], HALF);
+                tma_load_3d(sm + OFF_GB + gs * HALF, &tg, col0, c * CH, b, &sh.gfull[gs]);
+                issued = it + 1;
+            }
+            sh.g_issued = issued;
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t speer = sbase + OFF_SPEER, sown = sbase + OFF_SOWN;
-            for (int i = 0; i < n_own; ++i) {
-                const int s = i & 1;
-                const uint32_t u = static_cast<uint32_t>(i >> 1);
-                const uint32_t ph = static_cast<uint32_t>(i) & 1u;
-                if (!wait_bar(sh, p.status, &sh.kvready[s], u & 1u)) break;
-                if (!wait_bar(sh, p.status, &sh.qhfull, ph)) break;
+            int seen = 0;
+            for (int it = 0; it < total; ++it) {
+                const int s = it & 1;
+                const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
+                const uint32_t par = static_cast<uint32_t>(it) & 1u;
+                const int yb = it % kYBufs;
+                const uint32_t yph = static_cast<uint32_t>(it / kYBufs) & 1u;
+                if (!wait_bar(sh, p.status, &sh.actdone[s], ph)) break;
+                if (!wait_bar(sh, p.status, &sh.xin[s], ph)) break;
+                seen = it + 1;
+                if (!wait_bar(sh, p.status, &sh.aempty[s], ph ^ 1u)) break;
                 tc_fence_after();
-                const uint32_t ka = sbase + OFF_K + s * TILE, va = sbase + OFF_V + s * TILE;
-                // scores A = Q^ K^T
+                const uint32_t qa = sbase + OFF_QB + s * TILE, ka = sbase + OFF_KB + s * TILE;
+                const uint32_t va = sbase + OFF_VB + s * HALF, sb = sbase + OFF_SB;
+                const uint32_t tA = tm + TM_A + s * 128, tY = tm + TM_Y + yb * DV;
+                // scores A = Q^ K^T (128 x 128)
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_ts(tm + TM_A, tm + TM_Q + ks * 8,
-                           smem_desc_sw128(ka + (ks >> 2) * HALF + (ks & 3) * 32, 16, 1024),
-                           IDESC_QK, ks > 0);
-                mma_commit(&sh.afull);
-                if (!wait_bar(sh, p.status, &sh.yempty, ph ^ 1u)) break;
-                if (!wait_bar(sh, p.status, &sh.sownfull, ph)) break;
+                    mma_ss(tA, desc_kmajor(qa, ks), desc_kmajor(ka, ks), IDESC_QK, ks > 0);
+                mma_commit(&sh.afull[s]);
+                if (!wait_bar(sh, p.status, &sh.yempty[yb], yph ^ 1u)) break;
+                if (!wait_bar(sh, p.status, &sh.sready, par)) break;
                 tc_fence_after();
-                // Y = Q^ S_own
+                // Y = Q^ S_{<c}  (this CTA's 64 columns)
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_ts(tm + TM_Y, tm + TM_Q + ks * 8,
-                           smem_desc_sw128(sown + ks * 2048, HALF, 1024), IDESC_XB, ks > 0);
-                // S_own += K^T V
+                    mma_ss(tY, desc_kmajor(qa, ks), desc_mnmajor(sb, ks), IDESC_QS, ks > 0);
+                // S += K^T V  (fp32 in TMEM)
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_ss(tm + TM_S, smem_desc_sw128(ka + ks * 2048, HALF, 1024),
-                           smem_desc_sw128(va + ks * 2048, HALF, 1024), IDESC_KV, 1u);
+                    mma_ss(tm + TM_S, desc_mnmajor(ka, ks), desc_mnmajor(va, ks), IDESC_KV, 1u);
                 mma_commit(&sh.sdone);
-                if (!wait_bar(sh, p.status, &sh.speerfull, ph)) break;
-                if (i + 1 < n_own) mbar_arrive_expect_tx(&sh.speerfull, TILE);
+                if (!wait_bar(sh, p.status, &sh.pfull, par)) break;
                 tc_fence_after();
-                // Y += Q^ S_peer
+                // Y += P V^, P = mask(A) in bf16 over the first 64 columns of A
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_ts(tm + TM_Y, tm + TM_Q + ks * 8,
-                           smem_desc_sw128(speer + ks * 2048, HALF, 1024), IDESC_XB, 1u);
-                mma_commit_multicast(&sh.peercons, static_cast<uint16_t>(1u << peer));
-                mma_commit(&sh.qhempty);
-                if (!wait_bar(sh, p.status, &sh.pfull, ph)) break;
-                tc_fence_after();
-                // Y += mask(A) V^
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_ts(tm + TM_Y, tm + TM_P + ks * 8,
-                           smem_desc_sw128(va + ks * 2048, HALF, 1024), IDESC_XB, 1u);
-                mma_commit(&sh.yfull);
-                mma_commit(&sh.kvempty[s]);
+                    mma_ts(tY, tA + ks * 8, desc_mnmajor(va, ks), IDESC_PV, 1u);
+                mma_commit(&sh.yfull[yb]);
+                mma_commit(&sh.aempty[s]);
+                mma_commit_multicast(&sh.empty[s], static_cast<uint16_t>(3u));
             }
+            sh.xin_seen = seen;
             mma_commit(&sh.mmadone);
             wait_bar(sh, p.status, &sh.mmadone, 0, false, kDrainNs);
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ------------------------------------------------ transform warpgroup
-        const int q4 = warp - 4;
-        const int t = q4 * 32 + lane;  // token row (q, k, v, A, P) or d_k row (S)
+    } else if (warp == 2 || warp == 3) {
+        // ------------------------------------------------ publishers (CTA 0): the head's
+        // per-token sums of squares into the exchange slot, then the slot's counter.
+        // Warps 2 and 3 take alternate chunks.
+        if (rank == 0) {
+            for (int it = warp - 2; it < total; it += 2) {
+                const int xslot = it % kPairSlots;
+                const uint32_t xph = static_cast<uint32_t>(it / kPairSlots) & 1u;
+                int ok = 1;
+                if (lane == 0)
+                    ok = wait_bar(sh, p.status, &sh.ssown[xslot], xph) &&
+                         wait_bar<true>(sh, p.status, &sh.ssx[xslot], xph);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                while (!mbar_try_wait(&sh.ssown[xslot], xph)) {
+                }
+                while (!mbar_try_wait_acq_cluster(&sh.ssx[xslot], xph)) {
+                }
+                float* dst = p.xch + static_cast<size_t>(it) * CH * H + h;
+#pragma unroll
+                for (int k = 0; k < CH / 32; ++k) {
+                    const int t = lane + 32 * k;
+                    dst[static_cast<size_t>(t) * H] = sh.own[xslot][t] + sh.xs[xslot][t];
+                }
+                __syncwarp();
+                if (lane == 0) red_release_gpu_add(p.cnt + it, 1u);
+            }
+        }
+    } else if (warp >= 4 && warp < 12) {
+        // ------------------------------------------------ SiLU (two warpgroups)
+        const int t = (tid - 128) & 127;   // tile row (token)
+        const int part = (tid - 128) >> 7; // 0: own-tile half 0 + v chunks 0-3; 1: the rest
+        const bool leader = tid == 128;
+        const uint32_t peer_own = map_to_rank(sbase + own_off, peer);
+        const uint32_t peer_xin = map_to_rank(smem_addr(&sh.xin[0]), peer);
+        for (int it = 0; it < total; ++it) {
+            const int s = it & 1;
+            const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
+            if (!group_wait(sh, p.status, &sh.rawfull[s], ph, leader, 1, 256, 0)) break;
+            uint8_t* blk = sm + own_off + s * TILE + part * HALF;
+            uint8_t* vt = sm + OFF_VB + s * HALF;
+            uint4 x[4];
+#pragma unroll
+            for (int g4 = 0; g4 < 2; ++g4) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    x[j] = *reinterpret_cast<const uint4*>(blk + swz(t, 4 * g4 + j));
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4*>(blk + swz(t, 4 * g4 + j)) = silu_chunk(x[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                x[j] = *reinterpret_cast<const uint4*>(vt + swz(t, 4 * part + j));
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint4*>(vt + swz(t, 4 * part + j)) = silu_chunk(x[j]);
+            fence_proxy_async_smem();
+            named_bar_sync(1, 256);
+            if (leader) {
+                mbar_arrive(&sh.actdone[s]);
+                bulk_copy_to_peer(peer_own + s * TILE, sbase + own_off + s * TILE, TILE,
+                                  peer_xin + s * 8);
+            }
+        }
+    } else if (warp >= 12 && warp < 16) {
+        // ------------------------------------------------ state conversion + mask
+        const int q4 = warp & 3;
+        const int t = q4 * 32 + lane;  // token row (A, P) or d_k row (S)
         const bool leader = t == 0;
         const uint32_t lb = tm + (static_cast<uint32_t>(q4 * 32) << 16);
-        // initial state: S_in for rank 0 (or zeros), zeros for rank 1
-        {
-            const float* src =
-                (rank == 0 && p.S_in) ? p.S_in + (static_cast<size_t>(item) * D + t) * D : nullptr;
-#pragma unroll
-            for (int part = 0; part < 4; ++part) {
-                uint32_t r[32];
-#pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    float4 f = src ? *reinterpret_cast<const float4*>(src + 32 * part + j)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-                    r[j] = __float_as_uint(f.x);
-                    r[j + 1] = __float_as_uint(f.y);
-                    r[j + 2] = __float_as_uint(f.z);
-                    r[j + 3] = __float_as_uint(f.w);
-                }
-                LA_TMEM_ST32(lb + TM_S + 32 * part, r);
-                store_row_bf16(sm + OFF_SOWN, t, part, r);
-            }
-            tmem_wait_st();
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        named_bar_sync(1, 128);
-        int sends = 0, consumed = 0;
-        const uint32_t peer_speer = map_to_rank(sbase + OFF_SPEER, peer);
-        const uint32_t peer_bar = map_to_rank(smem_addr(&sh.speerfull), peer);
-        if (leader) {
-            mbar_arrive(&sh.sownfull);
-            if (rank == 1 && n_peer > 0)
-                bulk_copy_to_peer(peer_speer, sbase + OFF_SOWN, TILE, peer_bar);
-        }
-        if (rank == 1 && n_peer > 0) sends = 1;
-
-        for (int i = 0; i < n_own; ++i) {
-            const int s = i & 1;
-            const uint32_t u = static_cast<uint32_t>(i >> 1);
-            const uint32_t ph = static_cast<uint32_t>(i) & 1u;
-            // (1) q -> SiLU -> TMEM (A operand of the score and state products)
-            if (!group_wait(sh, p.status, &sh.qfull, ph, leader, 1, 128, 0)) break;
-            if (!group_wait(sh, p.status, &sh.qhempty, ph ^ 1u, leader, 1, 128, 0)) break;
-            tc_fence_after();
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                uint32_t r[32];
-                const uint8_t* tile = sm + OFF_Q + hf * HALF;
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    const uint4 v = silu_chunk(*reinterpret_cast<const uint4*>(tile + swz(t, cc)));
-                    r[4 * cc] = v.x;
-                    r[4 * cc + 1] = v.y;
-                    r[4 * cc + 2] = v.z;
-                    r[4 * cc + 3] = v.w;
-                }
-                LA_TMEM_ST32(lb + TM_Q + 32 * hf, r);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            named_bar_sync(1, 128);
-            if (leader) {
-                mbar_arrive(&sh.qhfull);
-                mbar_arrive(&sh.qempty);
-            }
-            // (2) k, v -> SiLU in place (operands of the score, state and P V products)
-            if (!group_wait(sh, p.status, &sh.kvfull[s], u & 1u, leader, 1, 128, 0)) break;
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                uint8_t* tile = sm + (m == 0 ? OFF_K : OFF_V) + s * TILE;
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) {
-                        uint4* pch = reinterpret_cast<uint4*>(tile + hf * HALF + swz(t, cc));
-                        *pch = silu_chunk(*pch);
-                    }
-            }
-            fence_proxy_async_smem();
-            named_bar_sync(1, 128);
-            if (leader) mbar_arrive(&sh.kvready[s]);
-            // (3) P = A masked to s <= t, packed bf16 into TMEM
-            if (!group_wait(sh, p.status, &sh.afull, ph, leader, 1, 128, 0)) break;
-            tc_fence_after();
-#pragma unroll
-            for (int part = 0; part < 4; ++part) {
-                uint32_t r[32];
-                LA_TMEM_LD32(lb + TM_A + 32 * part, r);
-                tmem_wait_ld();
-                uint32_t pk[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int s0 = 32 * part + 2 * j;
-                    const float lo = s0 <= t ? __uint_as_float(r[2 * j]) : 0.f;
-                    const float hi = s0 + 1 <= t ? __uint_as_float(r[2 * j + 1]) : 0.f;
-                    pk[j] = pack_bf16x2(lo, hi);
-                }
-                LA_TMEM_ST16(lb + TM_P + 16 * part, pk);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            named_bar_sync(1, 128);
-            if (leader) mbar_arrive(&sh.pfull);
-            // (4) bf16 copy of S_own for the next own chunk and for the peer
-            const bool send = rank == 0 ? (i < n_peer) : (i + 1 < n_peer);
-            if (i + 1 < n_own || send) {
-                if (!group_wait(sh, p.status, &sh.sdone, ph, leader, 1, 128, 0)) break;
-                if (sends > consumed) {
-                    if (!group_wait(sh, p.status, &sh.peercons,
-                                    static_cast<uint32_t>(consumed) & 1u, leader, 1, 128, 0))
-                        break;
-                    ++consumed;
-                }
+        uint8_t* sbk = sm + OFF_SB;
+        for (int it = 0; it <= total; ++it) {
+            const int b = it / Nc, c = it - b * Nc;
+            // (1) the bf16 operand S_{<c} for iteration it
+            if (it > 0) {
+                if (!group_wait(sh, p.status, &sh.sdone, static_cast<uint32_t>(it - 1) & 1u,
+                                leader, 2, 128, 1))
+                    break;
                 tc_fence_after();
+            }
+            if (c == 0) {
+                if (it > 0 && p.S_out) {  // the finished sequence's final state
+                    float* dst = p.S_out + ((static_cast<size_t>(b - 1) * H + h) * D + t) * D +
+                                 rank * DV;
 #pragma unroll
-                for (int part = 0; part < 4; ++part) {
+                    for (int part = 0; part < 2; ++part) {
+                        uint32_t r[32];
+                        LA_TMEM_LD32(lb + TM_S + 32 * part, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4*>(dst + 32 * part + j) =
+                                make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                            __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+                    }
+                }
+                if (it == total) break;
+                const float* src =
+                    p.S_in ? p.S_in + ((static_cast<size_t>(b) * H + h) * D + t) * D + rank * DV
+                           : nullptr;
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    uint32_t r[32];
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 f = src ? *reinterpret_cast<const float4*>(src + 32 * part + j)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                        r[j] = __float_as_uint(f.x);
+                        r[j + 1] = __float_as_uint(f.y);
+                        r[j + 2] = __float_as_uint(f.z);
+                        r[j + 3] = __float_as_uint(f.w);
+                    }
+                    LA_TMEM_ST32(lb + TM_S + 32 * part, r);
+                    store_row_bf16(sbk, t, part, r);
+                }
+                tmem_wait_st();
+            } else {
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
                     uint32_t r[32];
                     LA_TMEM_LD32(lb + TM_S + 32 * part, r);
                     tmem_wait_ld();
-                    store_row_bf16(sm + OFF_SOWN, t, part, r);
+                    store_row_bf16(sbk, t, part, r);
                 }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                named_bar_sync(1, 128);
-                if (leader) {
-                    mbar_arrive(&sh.sownfull);
-                    if (send) bulk_copy_to_peer(peer_speer, sbase + OFF_SOWN, TILE, peer_bar);
-                }
-                if (send) ++sends;
             }
-        }
-        // the peer must have consumed our last copy before either CTA exits
-        if (sends > consumed && leader)
-            wait_bar(sh, p.status, &sh.peercons, static_cast<uint32_t>(consumed) & 1u,
-                     !abort_set(sh), abort_set(sh) ? kDrainNs : kTimeoutNs);
-    } else if (warp >= 8) {
-        // ------------------------------------------------ epilogue (8 warps)
-        const int e = warp - 8;
-        const int q4 = e & 3, hf = e >> 2;  // TMEM lane quarter, column half
-        const int t = q4 * 32 + lane;
-        const int et = tid - 256;
-        const bool leader = et == 0;
-        const uint32_t lb = tm + (static_cast<uint32_t>(q4 * 32) << 16);
-        for (int i = 0; i < n_own; ++i) {
-            const int c = 2 * i + static_cast<int>(rank);
-            const int64_t row0 = static_cast<int64_t>(c) * CH;
-            const int64_t rem = p.N - row0;
-            const int nc = rem < CH ? static_cast<int>(rem) : CH;
-            const bool valid = t < nc;
-            const size_t grow =
-                ((static_cast<size_t>(b) * p.N + row0 + t) * p.H + h) * D + hf * 64;
-            if (!group_wait(sh, p.status, &sh.yfull, static_cast<uint32_t>(i) & 1u, leader, 2,
-                            256, 1))
-                break;
-            tc_fence_after();
-            uint32_t y[64];
-            LA_TMEM_LD32(lb + TM_Y + 64 * hf, y);
-            LA_TMEM_LD32(lb + TM_Y + 64 * hf + 32, (y + 32));
-            uint4 gv[8];
-            if (valid) {
-                const uint4* gp = reinterpret_cast<const uint4*>(p.g + grow);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) gv[j] = __ldg(gp + j);
-            }
-            tmem_wait_ld();
+            fence_proxy_async_smem();
             tc_fence_before();
+            named_bar_sync(2, 128);
+            if (leader) mbar_arrive(&sh.sready);
+            // (2) P = A masked to s <= t, bf16, written over the first 64 columns of A
+            const int a = it & 1;
+            const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
+            if (!group_wait(sh, p.status, &sh.afull[a], ph, leader, 2, 128, 1)) break;
+            tc_fence_after();
+            const uint32_t tA = lb + TM_A + a * 128;
+#pragma unroll
+            for (int part = 0; part < 4; ++part) {
+                uint32_t pk[16];
+                if (32 * part <= q4 * 32 + 31) {  // some lane of this warp has s <= t here
+                    uint32_t r[32];
+                    LA_TMEM_LD32(tA + 32 * part, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int s0 = 32 * part + 2 * j;
+                        const float lo = s0 <= t ? __uint_as_float(r[2 * j]) : 0.f;
+                        const float hi = s0 + 1 <= t ? __uint_as_float(r[2 * j + 1]) : 0.f;
+                        pk[j] = pack_bf16x2(lo, hi);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) pk[j] = 0u;
+                }
+                // columns [16 part, 16 part + 16) of A were read in an earlier or this part
+                LA_TMEM_ST16(tA + 16 * part, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            named_bar_sync(2, 128);
+            if (leader) mbar_arrive(&sh.pfull);
+        }
+    } else if (warp >= 16 && warp < 20) {
+        // ------------------------------------------------ post: per-token sums of squares
+        // into this CTA's slot (CTA 0) or into CTA 0's peer slot (CTA 1)
+        const int q4 = warp & 3;
+        const int t = q4 * 32 + lane;  // token row
+        const bool leader = t == 0;
+        const uint32_t lb = tm + (static_cast<uint32_t>(q4 * 32) << 16);
+        const uint32_t peer_xs = map_to_rank(smem_addr(&sh.xs[0][0]), peer);
+        const uint32_t peer_ssx = map_to_rank(smem_addr(&sh.ssx[0]), peer);
+        for (int it = 0; it < total; ++it) {
+            const int yb = it % kYBufs;
+            const uint32_t yph = static_cast<uint32_t>(it / kYBufs) & 1u;
+            if (!group_wait(sh, p.status, &sh.yfull[yb], yph, leader, 3, 128, 2)) break;
+            tc_fence_after();
             float ss = 0.f;
 #pragma unroll
-            for (int j = 0; j < 64; ++j)
-                ss = fmaf(__uint_as_float(y[j]), __uint_as_float(y[j]), ss);
-            sh.red[hf][t] = ss;
-            named_bar_sync(2, 256);
-            if (leader) mbar_arrive(&sh.yempty);
-            // partial sums of squares of chunk c: [token t][head], H floats per token
-            float* slot = p.xch + (static_cast<size_t>(b) * Nc + c) * CH * p.H;
-            if (hf == 0) {
-                slot[static_cast<size_t>(t) * p.H + h] = sh.red[0][t] + sh.red[1][t];
-                __threadfence();
-            }
-            // while the other heads arrive: debug copy of y, then y *= sigmoid(g)
-            if (valid) {
-                if (p.y_dbg) {
-                    float4* yp = reinterpret_cast<float4*>(p.y_dbg + grow);
+            for (int part = 0; part < 2; ++part) {
+                uint32_t y[32];
+                LA_TMEM_LD32(lb + TM_Y + yb * DV + 32 * part, y);
+                tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        yp[j] = make_float4(__uint_as_float(y[4 * j]), __uint_as_float(y[4 * j + 1]),
-                                            __uint_as_float(y[4 * j + 2]),
-                                            __uint_as_float(y[4 * j + 3]));
-                }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t gw[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
-#pragma unroll
-                    for (int k2 = 0; k2 < 4; ++k2) {
-                        y[8 * j + 2 * k2] = __float_as_uint(__uint_as_float(y[8 * j + 2 * k2]) *
-                                                            sigmoid_fast(bf_lo(gw[k2])));
-                        y[8 * j + 2 * k2 + 1] = __float_as_uint(
-                            __uint_as_float(y[8 * j + 2 * k2 + 1]) * sigmoid_fast(bf_hi(gw[k2])));
-                    }
-                }
+                for (int j = 0; j < 32; ++j)
+                    ss = fmaf(__uint_as_float(y[j]), __uint_as_float(y[j]), ss);
             }
-            named_bar_sync(2, 256);
-            if (leader) {
-                unsigned* cp = p.cnt + static_cast<size_t>(b) * Nc + c;
-                red_release_gpu_add(cp, 1u);
-                int ok = 1;
-                uint64_t t0 = 0;
-                for (uint32_t it = 0;; ++it) {
-                    if (ld_acquire_gpu(cp) >= static_cast<unsigned>(p.H)) break;
-                    if ((it & 63u) == 63u) {
-                        if (abort_set(sh)) { ok = 0; break; }
-                        const uint64_t now = global_timer_ns();
-                        if (t0 == 0) t0 = now;
-                        else if (now - t0 > kTimeoutNs) { raise_abort(sh, p.status); ok = 0; break; }
-                    }
-                }
-                sh.verdict[1] = ok;
+            const int xslot = it % kPairSlots;
+            if (rank == 1) {
+                st_cluster_f32(peer_xs + static_cast<uint32_t>((xslot * CH + t) * 4), ss);
+                mbar_arrive_remote(peer_ssx + xslot * 8);
+            } else {
+                sh.own[xslot][t] = ss;
+                mbar_arrive(&sh.ssown[xslot]);
             }
-            named_bar_sync(2, 256);
-            if (!*reinterpret_cast<volatile int*>(&sh.verdict[1])) break;
+        }
+    } else if (warp >= 20) {
+        // ------------------------------------------------ finish: norm, gate, store
+        const int fg = (warp - 20) >> 2;  // 0 or 1: even or odd iterations
+        const int q4 = warp & 3;
+        const int t = q4 * 32 + lane;     // token row
+        const bool leader = t == 0;
+        const uint32_t bar_id = 4 + fg;
+        const int slot = 3 + fg;
+        const uint32_t lb = tm + (static_cast<uint32_t>(q4 * 32) << 16);
+        for (int it = fg; it < total; it += 2) {
+            const int b = it / Nc, c = it - b * Nc;
+            const int yb = it % kYBufs;
+            const uint32_t yph = static_cast<uint32_t>(it / kYBufs) & 1u;
+            const int gs = it % kGBufs;
+            const uint32_t gph = static_cast<uint32_t>(it / kGBufs) & 1u;
+            const int64_t tok = static_cast<int64_t>(c) * CH + t;
+            const bool valid = tok < p.N;
+            const size_t grow = (static_cast<size_t>(b) * p.N + tok) * H * D + col0;
+            // every head has posted this chunk (bounded wait on the counter)
+            if (leader) sh.verdict[slot] = spin_counter(sh, p.status, p.cnt + it, H) ? 1 : 0;
+            named_bar_sync(bar_id, 128);
+            if (!*reinterpret_cast<volatile int*>(&sh.verdict[slot])) break;
+            // r_t from the H head sums of token t, in head order (one batch of loads)
+            float acc = 0.f;
             {
-                // half hf sums heads [hh0, hh1) of token t; the loads are issued together
-                const int hh0 = hf * (p.H / 2), hh1 = hf == 0 ? p.H / 2 : p.H;
-                const float* src = slot + static_cast<size_t>(t) * p.H;
-                float acc = 0.f;
-                if ((p.H & 7) == 0) {
-                    const float4* s4 = reinterpret_cast<const float4*>(src + hh0);
-                    const int n4 = (hh1 - hh0) >> 2;
+                const float* src = p.xch + (static_cast<size_t>(it) * CH + t) * H;
+                if (H == 64) {
+                    const float4* s4 = reinterpret_cast<const float4*>(src);
+                    float4 v[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] = __ldcg(s4 + j);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) acc += ((v[j].x + v[j].y) + (v[j].z + v[j].w));
+                } else if ((H & 3) == 0) {
+                    const float4* s4 = reinterpret_cast<const float4*>(src);
+                    const int n4 = H >> 2;
                     for (int base = 0; base < n4; base += 8) {
                         float4 v[8];
 #pragma unroll
@@ -560,79 +636,74 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j = 0; j < 8; ++j) acc += ((v[j].x + v[j].y) + (v[j].z + v[j].w));
                     }
                 } else {
-                    for (int base = hh0; base < hh1; base += 16) {
+                    for (int base = 0; base < H; base += 16) {
                         float v[16];
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) v[j] = base + j < hh1 ? __ldcg(src + base + j) : 0.f;
+                        for (int j = 0; j < 16; ++j) v[j] = base + j < H ? __ldcg(src + base + j) : 0.f;
 #pragma unroll
                         for (int j = 0; j < 16; ++j) acc += v[j];
                     }
                 }
-                sh.red[hf][t] = acc;
             }
-            named_bar_sync(2, 256);
-            if (hf == 0) sh.rnorm[t] = rsqrtf((sh.red[0][t] + sh.red[1][t]) * p.inv_width + p.eps);
-            named_bar_sync(2, 256);
-            const float rn = sh.rnorm[t];
-            if (valid) {
-                uint4* op = reinterpret_cast<uint4*>(p.out + grow);
+            const float rn = rsqrtf(acc * p.inv_width + p.eps);
+            // out = y (fp32, TMEM) * r_t * sigmoid(g) (g from the TMA-loaded tile)
+            if (!group_wait(sh, p.status, &sh.gfull[gs], gph, leader, bar_id, 128, slot)) break;
+            if (!group_wait(sh, p.status, &sh.yfull[yb], yph, leader, bar_id, 128, slot)) break;
+            tc_fence_after();
+            const uint8_t* gt = sm + OFF_GB + gs * HALF;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint32_t ow[4];
+            for (int part = 0; part < 2; ++part) {
+                uint32_t y[32];
+                LA_TMEM_LD32(lb + TM_Y + yb * DV + 32 * part, y);
+                tmem_wait_ld();
+                if (p.y_dbg && valid) {
+                    float4* yp = reinterpret_cast<float4*>(p.y_dbg + grow + 32 * part);
 #pragma unroll
-                    for (int k2 = 0; k2 < 4; ++k2)
-                        ow[k2] = pack_bf16x2(__uint_as_float(y[8 * j + 2 * k2]) * rn,
-                                             __uint_as_float(y[8 * j + 2 * k2 + 1]) * rn);
-                    op[j] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                    for (int j = 0; j < 8; ++j)
+                        yp[j] = make_float4(__uint_as_float(y[4 * j]), __uint_as_float(y[4 * j + 1]),
+                                            __uint_as_float(y[4 * j + 2]),
+                                            __uint_as_float(y[4 * j + 3]));
                 }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 gv = *reinterpret_cast<const uint4*>(gt + swz(t, 4 * part + j));
+                    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+                    uint32_t w[4];
+#pragma unroll
+                    for (int k2 = 0; k2 < 4; ++k2) {
+                        const float y0 = __uint_as_float(y[8 * j + 2 * k2]) * rn;
+                        const float y1 = __uint_as_float(y[8 * j + 2 * k2 + 1]) * rn;
+                        w[k2] = pack_bf16x2(y0 * sigmoid_t(bf_lo(gw[k2])),
+                                            y1 * sigmoid_t(bf_hi(gw[k2])));
+                    }
+                    if (valid)
+                        reinterpret_cast<uint4*>(p.out + grow)[4 * part + j] =
+                            make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            tc_fence_before();
+            named_bar_sync(bar_id, 128);
+            if (leader) {
+                mbar_arrive(&sh.yempty[yb]);
+                mbar_arrive(&sh.gempty[gs]);
             }
         }
     }
 
-    // ---------------------------------------------------- final state S_0 + S_1
+    // ---------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
-    tc_fence_after();
-    const bool ok_all = !abort_set(sh);
-    const bool combine = p.S_out != nullptr;
-    if (combine && rank == 1 && warp >= 4 && warp < 8) {
-        const int q4 = warp - 4, t = q4 * 32 + lane;
-        const uint32_t lb = tm + (static_cast<uint32_t>(q4 * 32) << 16);
-        float* row = reinterpret_cast<float*>(sm + OFF_K + t * 512);
-#pragma unroll
-        for (int part = 0; part < 4; ++part) {
-            uint32_t r[32];
-            LA_TMEM_LD32(lb + TM_S + 32 * part, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4*>(row + 32 * part + j) =
-                    make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-        }
+    if (tid == 0) {
+        // abort paths only: copies that were announced but not consumed land first
+        for (int it = sh.xin_seen; it < sh.issued; ++it)
+            wait_bar(sh, p.status, &sh.xin[it & 1], static_cast<uint32_t>(it >> 1) & 1u, false,
+                     kDrainNs);
+        for (int it = sh.g_issued - kGBufs < 0 ? 0 : sh.g_issued - kGBufs; it < sh.g_issued; ++it)
+            wait_bar(sh, p.status, &sh.gfull[it % kGBufs],
+                     static_cast<uint32_t>(it / kGBufs) & 1u, false, kDrainNs);
     }
-    cluster_sync();
-    if (combine && ok_all && rank == 0 && warp >= 4 && warp < 8) {
-        const int q4 = warp - 4, t = q4 * 32 + lane;
-        const uint32_t lb = tm + (static_cast<uint32_t>(q4 * 32) << 16);
-        const uint32_t prow = map_to_rank(sbase + OFF_K + t * 512, peer);
-        float* dst = p.S_out + (static_cast<size_t>(item) * D + t) * D;
-#pragma unroll
-        for (int part = 0; part < 4; ++part) {
-            uint32_t r[32];
-            LA_TMEM_LD32(lb + TM_S + 32 * part, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                const float4 o = ld_cluster_f4(prow + (32 * part + j) * 4);
-                *reinterpret_cast<float4*>(dst + 32 * part + j) =
-                    make_float4(__uint_as_float(r[j]) + o.x, __uint_as_float(r[j + 1]) + o.y,
-                                __uint_as_float(r[j + 2]) + o.z, __uint_as_float(r[j + 3]) + o.w);
-            }
-        }
-    }
-    tc_fence_before();
-    cluster_sync();
+    __syncthreads();
+    cluster_sync();  // no copy or remote arrival targets a CTA that has left
     tc_fence_after();
     if (warp == 2) tmem_dealloc(tm, 512);
 }
@@ -658,7 +729,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 }
 
 // [B][N][H*d] bf16 as a 3-D tensor (x = feature, y = token, z = sequence); boxes of
-// 64 features x 128 tokens, 128B swizzle; tokens past N read as zero.
+// 64 features x 128 tokens, 128B swizzle; loads past N read zeros, stores past N are
+// dropped.
 bool encode_io_map(CUtensorMap* m, const void* base, int B, int H, int64_t N) {
     auto enc = encoder();
     if (!enc) return false;
@@ -705,37 +777,37 @@ int max_active_clusters() {
 
 int prefill_tc_supported(int B, int H, int64_t N) {
     if (N <= 0 || N > (int64_t(1) << 30)) return LA_ERR_UNSUPPORTED;
+    const int64_t Nc = (N + CH - 1) / CH;
+    if (static_cast<int64_t>(B) * Nc > kTcCounterSlots) return LA_ERR_UNSUPPORTED;
     if (!encoder()) return LA_ERR_UNSUPPORTED;
     const int mc = max_active_clusters();
-    // every (b, h) pair must be resident at once for the cross-head exchange
-    if (mc <= 0 || static_cast<int64_t>(B) * H > mc) return LA_ERR_UNSUPPORTED;
+    // every head's pair must be resident at once for the cross-head exchange
+    if (mc <= 0 || H > mc) return LA_ERR_UNSUPPORTED;
     return LA_OK;
 }
 
 size_t prefill_tc_workspace_bytes(int B, int H, int64_t N) {
     const int64_t Nc = (N + CH - 1) / CH;
-    const size_t xch = static_cast<size_t>(B) * Nc * H * CH * sizeof(float);
-    const size_t cnt = (static_cast<size_t>(B) * Nc * sizeof(unsigned) + 255) & ~size_t(255);
-    return xch + cnt;
+    return static_cast<size_t>(B) * Nc * CH * H * sizeof(float);
 }
 
 int launch_prefill_tc(const void* q, const void* k, const void* v, const void* g, void* out,
                       const float* S_in, float* S_out, float* y_debug, int B, int H, int64_t N,
                       float eps, const Workspace& ws, cudaStream_t st) {
     const int64_t Nc = (N + CH - 1) / CH;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mg;
     if (!encode_io_map(&mq, q, B, H, N) || !encode_io_map(&mk, k, B, H, N) ||
-        !encode_io_map(&mv, v, B, H, N))
+        !encode_io_map(&mv, v, B, H, N) || !encode_io_map(&mg, g, B, H, N))
         return LA_ERR_UNSUPPORTED;
     Params prm;
-    prm.g = static_cast<const __nv_bfloat16*>(g);
     prm.out = static_cast<__nv_bfloat16*>(out);
     prm.S_in = S_in;
     prm.S_out = S_out;
     prm.y_dbg = y_debug;
-    const size_t xch_bytes = static_cast<size_t>(B) * Nc * H * CH * sizeof(float);
     prm.xch = static_cast<float*>(ws.base);
-    prm.cnt = reinterpret_cast<unsigned*>(static_cast<char*>(ws.base) + xch_bytes);
+    prm.cnt = ws.banks + (ws.bank & 1u) * kTcCounterSlots;
+    prm.cnt_clear = ws.banks + ((ws.bank & 1u) ^ 1u) * kTcCounterSlots;
+    prm.n_clear = kTcCounterSlots;
     prm.status = ws.status;
     prm.B = B;
     prm.H = H;
@@ -743,11 +815,8 @@ int launch_prefill_tc(const void* q, const void* k, const void* v, const void* g
     prm.Nc = static_cast<int>(Nc);
     prm.eps = eps;
     prm.inv_width = 1.0f / static_cast<float>(H * D);
-    if (cudaMemsetAsync(prm.cnt, 0, static_cast<size_t>(B) * Nc * sizeof(unsigned), st) !=
-        cudaSuccess)
-        return LA_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * B * H), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * H), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = SMEM_DYN;
     cfg.stream = st;
@@ -758,10 +827,11 @@ int launch_prefill_tc(const void* q, const void* k, const void* v, const void* g
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, k_prefill_tc, mq, mk, mv, prm) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, k_prefill_tc, mq, mk, mv, mg, prm) != cudaSuccess) {
         cudaGetLastError();
         return LA_ERR_CUDA;
     }
+    workspace_switch_bank();
     note_launches(1);
     return LA_OK;
 }

@@ -8,7 +8,8 @@
 //    CUDA-core alternative to the tensor-core kernel.
 //  * k_norm_gate_rows: step 4 of the mechanism, RMSNorm over the H*d features of a
 //    token times sigmoid(g), one CTA per token row.
-//  * k_decode_state / k_decode_norm: one-token decode against the carried state.
+//  * k_decode_step: one-token decode against the carried state, with the norm over
+//    all heads of a sequence fused in (the last head of each sequence applies it).
 //
 // All accumulation is fp32; SiLU and sigmoid use the accurate expf.
 #include <cuda_bf16.h>
@@ -198,19 +199,30 @@ __global__ void __launch_bounds__(256) k_norm_gate_rows(const float* __restrict_
 }
 
 // Decode: one CTA per (b,h), 256 threads; thread (rg, jc) streams rows i = rg + 8 r of
-// the 128 x 128 fp32 state as float4 columns 4 jc .. 4 jc + 3.
+// the 128 x 128 fp32 state as float4 columns 4 jc .. 4 jc + 3, updates them in place
+// (S += k^T v) and accumulates y = q S.  The CTA then publishes y and its sum of squares
+// and bumps the arrival counter of sequence b; the last of the H heads of b to arrive
+// applies the norm over all H*d features of b and the gate (no CTA ever waits, so the
+// order in which CTAs run does not matter).  The last CTA also resets the counter, so
+// the counters are zero between calls.
 template <typename T>
-__global__ void __launch_bounds__(256) k_decode_state(float* __restrict__ S,
-                                                      const T* __restrict__ q,
-                                                      const T* __restrict__ k,
-                                                      const T* __restrict__ v,
-                                                      float* __restrict__ y,
-                                                      float* __restrict__ ss) {
+__global__ void __launch_bounds__(256) k_decode_step(float* __restrict__ S,
+                                                     const T* __restrict__ q,
+                                                     const T* __restrict__ k,
+                                                     const T* __restrict__ v,
+                                                     const T* __restrict__ g,
+                                                     T* __restrict__ out, float* __restrict__ y,
+                                                     float* __restrict__ ss,
+                                                     unsigned* __restrict__ cnt, int H,
+                                                     float eps) {
     __shared__ float qs[D], ks[D];
     __shared__ __align__(16) float vs[D];
     __shared__ float4 red[8][32];
+    __shared__ float rsh[8];
+    __shared__ int last;
     const int tid = threadIdx.x;
     const int64_t bh = blockIdx.x;
+    const int64_t b = bh / H;
     if (tid < D) {
         const int64_t off = bh * D + tid;
         qs[tid] = silu_f(ldf(q, off));
@@ -248,21 +260,29 @@ __global__ void __launch_bounds__(256) k_decode_state(float* __restrict__ S,
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
         if (tid == 0) ss[bh] = p;
+        __threadfence();  // y and ss are visible device-wide before the arrival below
     }
-}
-
-// Decode norm: grid (B, H), 128 threads; r from the H per-head partial sums of b.
-template <typename T>
-__global__ void __launch_bounds__(128) k_decode_norm(const float* __restrict__ y,
-                                                     const float* __restrict__ ss,
-                                                     const T* __restrict__ g,
-                                                     T* __restrict__ out, int H, float eps) {
-    const int64_t b = blockIdx.x, h = blockIdx.y;
-    float s = 0.f;
-    for (int i = 0; i < H; ++i) s += ss[b * H + i];  // fixed order
-    const float r = rsqrtf(s / (float)(H * D) + eps);
-    const int64_t off = (b * H + h) * D + threadIdx.x;
-    stf(out, off, y[off] * r * sigmoid_f(ldf(g, off)));
+    __syncthreads();
+    if (tid == 0) last = atomicAdd(cnt + b, 1u) == static_cast<unsigned>(H - 1);
+    __syncthreads();
+    if (!last) return;
+    // ---- the last head of sequence b: norm over the H*d features, then the gate
+    __threadfence();
+    float part = 0.f;
+    for (int i = tid; i < H; i += 256) part += __ldcg(ss + b * H + i);
+    // fixed-order reduction (deterministic): warp tree, then the 8 warps in order
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if ((tid & 31) == 0) rsh[tid >> 5] = part;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += rsh[w];
+    const float r = rsqrtf(tot / static_cast<float>(H * D) + eps);
+    const int64_t base = b * H * D;
+    for (int64_t e = tid; e < static_cast<int64_t>(H) * D; e += 256)
+        stf(out, base + e, __ldcg(y + base + e) * r * sigmoid_f(ldf(g, base + e)));
+    if (tid == 0) cnt[b] = 0u;
 }
 
 __global__ void k_zero(float* p, int64_t n) {
@@ -311,23 +331,18 @@ int launch_norm_gate_rows(const float* y, const void* g, void* out, int64_t rows
 }
 
 int launch_decode(float* S, const void* q, const void* k, const void* v, const void* g,
-                  void* out, float* y, float* ss, int B, int H, float eps, bool bf16,
-                  cudaStream_t st) {
+                  void* out, float* y, float* ss, unsigned* cnt, int B, int H, float eps,
+                  bool bf16, cudaStream_t st) {
     const unsigned nbh = (unsigned)((int64_t)B * H);
-    dim3 ngrid(B, H);
-    if (bf16) {
-        k_decode_state<__nv_bfloat16><<<nbh, 256, 0, st>>>(
-            S, (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, y,
-            ss);
-        k_decode_norm<__nv_bfloat16><<<ngrid, 128, 0, st>>>(y, ss, (const __nv_bfloat16*)g,
-                                                            (__nv_bfloat16*)out, H, eps);
-    } else {
-        k_decode_state<float><<<nbh, 256, 0, st>>>(S, (const float*)q, (const float*)k,
-                                                   (const float*)v, y, ss);
-        k_decode_norm<float><<<ngrid, 128, 0, st>>>(y, ss, (const float*)g, (float*)out, H,
-                                                    eps);
-    }
-    note_launches(2);
+    if (bf16)
+        k_decode_step<__nv_bfloat16><<<nbh, 256, 0, st>>>(
+            S, (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v,
+            (const __nv_bfloat16*)g, (__nv_bfloat16*)out, y, ss, cnt, H, eps);
+    else
+        k_decode_step<float><<<nbh, 256, 0, st>>>(S, (const float*)q, (const float*)k,
+                                                  (const float*)v, (const float*)g,
+                                                  (float*)out, y, ss, cnt, H, eps);
+    note_launches(1);
     return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 

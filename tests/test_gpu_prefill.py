@@ -97,39 +97,60 @@ def test_prefill_8k_workload_full(env):
     _check_prefill(env, w.B, w.N, w.H, "bf16", w.scale, w.seed, simt=False)
 
 
-def test_prefill_128k_workload_windows(env):
-    """B1 H64 N131072: the oracle runs the state pass up to two seeded 4096-token
-    windows (all heads, since the norm spans them) and checks those windows and the
-    final state."""
+def _check_long_windows(env, name, n_windows, slab=8192):
+    """Long prefill: the whole sequence runs on the GPU; the oracle carries the fp64
+    state through the sequence in slabs (oracle.state_pass, all heads) and runs the
+    full layer on ``n_windows`` seeded 4096-token windows from the state at each
+    window's start.  Each window is checked on all heads (the norm spans them) and on
+    one seeded head; the final state on every head."""
     torch, la, orc = env
+    from oracle.state_pass import state_pass
     from linear_attention_hybrid_fwd_b300.inputs import WORKLOADS
-    w = WORKLOADS["prefill_128k"]
+    w = WORKLOADS[name]
     q, k, v, g = _inputs(torch, w.B, w.N, w.H, torch.bfloat16, w.scale, w.seed)
     out, S = la.la_prefill(q, k, v, g)
     torch.cuda.synchronize()
     assert la.la_get_device_status() == 0
+    assert la.la_prefill_path(w.B, w.H, w.N) == 0
     rng = np.random.default_rng(w.seed)
     W = 4096
-    starts = sorted(int(s) for s in rng.integers(0, w.N - W, size=2))
-    S_run = np.zeros((1, w.H, 128, 128))
+    starts = sorted(int(s) for s in rng.integers(0, w.N - W, size=n_windows))
+    heads = [int(x) for x in rng.integers(0, w.H, size=n_windows)]
+    S_run = np.zeros((w.B, w.H, 128, 128))
     pos = 0
-    slab = 8192
-    for t0 in starts + [w.N]:
-        while pos < t0:  # state-only pass over [pos, t0) in slabs
+    for t0, hsel in zip(starts + [w.N], heads + [None]):
+        while pos < t0:  # state-only pass over [pos, t0)
             e = min(t0, pos + slab)
-            kh = orc.silu(host64(k[:, pos:e]))
-            vh = orc.silu(host64(v[:, pos:e]))
-            _, S_run = orc.core(kh, kh, vh, S0=S_run, want_y=False)
+            S_run = state_pass(k[:, pos:e].cpu(), v[:, pos:e].cpu(), S_run)
             pos = e
-        if t0 == w.N:
+        if hsel is None:
             break
         sl = slice(t0, t0 + W)
         ref_out, _, _ = orc.prefill(host64(q[:, sl]), host64(k[:, sl]), host64(v[:, sl]),
                                     host64(g[:, sl]), S0=S_run)
-        e_out = rel_max_err(host64(out[:, sl]), ref_out)
-        assert e_out <= TOL["bf16"]["out"], f"window {t0}: out rel err {e_out:.3e}"
+        got = host64(out[:, sl])
+        e_all = rel_max_err(got, ref_out)
+        e_head = rel_max_err(got[:, :, hsel], ref_out[:, :, hsel])
+        assert e_all <= TOL["bf16"]["out"], f"window {t0}: out rel err {e_all:.3e}"
+        assert e_head <= TOL["bf16"]["out"], f"window {t0} head {hsel}: {e_head:.3e}"
     e_S = rel_max_err(host64(S), S_run)
     assert e_S <= TOL["bf16"]["state"], f"final state rel err {e_S:.3e}"
+    for h in range(w.H):
+        assert rel_max_err(host64(S[:, h]), S_run[:, h]) <= TOL["bf16"]["state"], h
+
+
+def test_prefill_128k_workload_windows(env):
+    """B1 H64 N131072 d128 bf16: two seeded windows and the final state."""
+    _check_long_windows(env, "prefill_128k", 2)
+
+
+def test_prefill_1m_workload_windows(env):
+    """B1 H64 N1048576 d128 bf16 (about 84 GB of I/O): eight seeded (head, 4096-token
+    window) slices and the final per-head state."""
+    torch, _, _ = env
+    free, _ = torch.cuda.mem_get_info()
+    assert free > 100 * 2**30, "the 1M-token workload needs about 90 GB of device memory"
+    _check_long_windows(env, "prefill_1m", 8)
 
 
 @pytest.mark.parametrize("simt", [False, True])

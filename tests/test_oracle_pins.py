@@ -263,3 +263,28 @@ def test_threads_do_not_change_result(oracle_mod):
     y4, S4 = oracle_mod.core(qh, kh, vh, nthreads=4)
     np.testing.assert_array_equal(y1, y4)
     np.testing.assert_array_equal(S1, S4)
+
+
+# ------------------------------------------------------- long-sequence state pass
+def test_state_pass_matches_recurrence(oracle_mod):
+    """The batched-matmul state pass ends where the C token recurrence ends."""
+    from oracle.state_pass import state_pass
+    rng = np.random.default_rng(15)
+    B, N, H, d = 2, 77, 3, 16
+    q, k, v, g = (_rand(rng, (B, N, H, d)) for _ in range(4))
+    S0 = _rand(rng, (B, H, d, d))
+    _, _, S_rec = oracle_mod.prefill(q, k, v, g, S0=S0)
+    np.testing.assert_allclose(state_pass(k, v, S0), S_rec, rtol=1e-12, atol=1e-12)
+    # chained over slabs, as the long-sequence tests use it
+    S_run = None
+    for a in range(0, N, 20):
+        S_run = state_pass(k[:, a:a + 20], v[:, a:a + 20], S_run)
+    _, _, S_zero = oracle_mod.prefill(q, k, v, g)
+    np.testing.assert_allclose(S_run, S_zero, rtol=1e-12, atol=1e-12)
+
+
+def test_state_pass_silu_is_textbook():
+    from oracle.state_pass import silu64
+    x = np.linspace(-30, 30, 601)
+    np.testing.assert_allclose(silu64(x).numpy(), 0.5 * x * (1 + np.tanh(0.5 * x)),
+                               rtol=1e-13, atol=1e-14)
