@@ -40,6 +40,27 @@ template <> __device__ __forceinline__ void stf<__nv_bfloat16>(__nv_bfloat16* p,
     p[i] = __float2bfloat16_rn(x);
 }
 
+// Four consecutive elements at element offset i (a multiple of 4: 16- or 8-byte aligned).
+__device__ __forceinline__ float4 ld4(const float* p, int64_t i) {
+    return *reinterpret_cast<const float4*>(p + i);
+}
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16* p, int64_t i) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p + i);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+}
+__device__ __forceinline__ void st4(float* p, int64_t i, float4 v) {
+    *reinterpret_cast<float4*>(p + i) = v;
+}
+__device__ __forceinline__ void st4(__nv_bfloat16* p, int64_t i, float4 v) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&lo);
+    u.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(p + i) = u;
+}
+
 constexpr int D = kHeadDim;
 constexpr int C = 64;        // tokens per chunk
 constexpr int DV = 32;       // d_v columns per CTA (grid.y = D / DV)
@@ -206,7 +227,7 @@ __global__ void __launch_bounds__(256) k_norm_gate_rows(const float* __restrict_
 // order in which CTAs run does not matter).  The last CTA also resets the counter, so
 // the counters are zero between calls.
 template <typename T>
-__global__ void __launch_bounds__(256) k_decode_step(float* __restrict__ S,
+__global__ void __launch_bounds__(256, 3) k_decode_step(float* __restrict__ S,
                                                      const T* __restrict__ q,
                                                      const T* __restrict__ k,
                                                      const T* __restrict__ v,
@@ -280,8 +301,28 @@ __global__ void __launch_bounds__(256) k_decode_step(float* __restrict__ S,
     for (int w = 0; w < 8; ++w) tot += rsh[w];
     const float r = rsqrtf(tot / static_cast<float>(H * D) + eps);
     const int64_t base = b * H * D;
-    for (int64_t e = tid; e < static_cast<int64_t>(H) * D; e += 256)
-        stf(out, base + e, __ldcg(y + base + e) * r * sigmoid_f(ldf(g, base + e)));
+    // 4 consecutive features per thread and step; 4 steps' loads are issued together
+    const int n4 = H * (D / 4);
+    for (int k0 = tid; k0 < n4; k0 += 256 * 4) {
+        float4 yv[4];
+        float4 gv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int k = k0 + 256 * j;
+            if (k < n4) {
+                yv[j] = __ldcg(reinterpret_cast<const float4*>(y + base) + k);
+                gv[j] = ld4(g, base + 4 * static_cast<int64_t>(k));
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int k = k0 + 256 * j;
+            if (k < n4)
+                st4(out, base + 4 * static_cast<int64_t>(k),
+                    make_float4(yv[j].x * r * sigmoid_f(gv[j].x), yv[j].y * r * sigmoid_f(gv[j].y),
+                                yv[j].z * r * sigmoid_f(gv[j].z), yv[j].w * r * sigmoid_f(gv[j].w)));
+        }
+    }
     if (tid == 0) cnt[b] = 0u;
 }
 
