@@ -20,13 +20,27 @@ std::atomic<int64_t> g_launches{0};
 std::mutex g_ws_mutex;
 Workspace g_ws[kMaxDevices];
 
+struct XchState {
+    float* base = nullptr;   // 2 flag banks of `words` words
+    size_t words = 0;
+    unsigned bank = 0;       // the bank the next launch writes
+    size_t dirty[2] = {0, 0};
+    float* part = nullptr;   // partials
+    size_t part_floats = 0;
+};
+XchState g_xch[kMaxDevices];
+
 struct WorkspaceReaper {
     ~WorkspaceReaper() {
         // Process teardown: the driver may already be gone; ignore errors.
+        for (auto& x : g_xch) {
+            if (x.base) cudaFree(x.base);
+            if (x.part) cudaFree(x.part);
+        }
         for (auto& w : g_ws) {
             if (w.base) cudaFree(w.base);
             if (w.status) cudaFree(w.status);
-            if (w.banks) cudaFree(w.banks);
+            if (w.dec_cnt) cudaFree(w.dec_cnt);
         }
     }
 } g_reaper;
@@ -52,27 +66,25 @@ int workspace_acquire(size_t bytes, cudaStream_t st, Workspace* out) {
     Workspace& w = g_ws[dev];
     if (!w.status) {
         int* status = nullptr;
-        unsigned* banks = nullptr;
+        unsigned* cnt = nullptr;
         if (cudaMalloc(&status, 256) != cudaSuccess) {
             cudaGetLastError();
             return LA_ERR_NOMEM;
         }
-        const size_t cbytes = 2 * kTcCounterBytes + size_t(kDecodeCounterSlots) * sizeof(unsigned);
-        if (cudaMalloc(&banks, cbytes) != cudaSuccess) {
+        const size_t cbytes = size_t(kDecodeCounterSlots) * sizeof(unsigned);
+        if (cudaMalloc(&cnt, cbytes) != cudaSuccess) {
             cudaGetLastError();
             cudaFree(status);
             return LA_ERR_NOMEM;
         }
         if (cudaMemsetAsync(status, 0, 256, st) != cudaSuccess ||
-            cudaMemsetAsync(banks, 0, cbytes, st) != cudaSuccess) {
+            cudaMemsetAsync(cnt, 0, cbytes, st) != cudaSuccess) {
             cudaFree(status);
-            cudaFree(banks);
+            cudaFree(cnt);
             return LA_ERR_CUDA;
         }
         w.status = status;
-        w.banks = banks;
-        w.dec_cnt = banks + 2 * kTcCounterSlots;
-        w.bank = 0;
+        w.dec_cnt = cnt;
     }
     if (bytes > w.bytes) {
         // cudaFree waits for work already queued on the device, so a smaller
@@ -91,11 +103,57 @@ int workspace_acquire(size_t bytes, cudaStream_t st, Workspace* out) {
     return LA_OK;
 }
 
-void workspace_switch_bank() {
+int xch_acquire(size_t flag_words, size_t part_floats, cudaStream_t st, XchLease* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    XchState& x = g_xch[dev];
+    if (flag_words > x.words) {
+        if (x.base) cudaFree(x.base);  // waits for work already queued on the device
+        x.base = nullptr;
+        x.words = 0;
+        const size_t want = (flag_words + (size_t(1) << 16) - 1) & ~((size_t(1) << 16) - 1);
+        if (cudaMalloc(&x.base, 2 * want * sizeof(float)) != cudaSuccess) {
+            cudaGetLastError();
+            return LA_ERR_NOMEM;
+        }
+        // every word starts empty (kXchEmpty is the byte 0x80 repeated)
+        if (cudaMemsetAsync(x.base, 0x80, 2 * want * sizeof(float), st) != cudaSuccess) {
+            cudaFree(x.base);
+            x.base = nullptr;
+            return LA_ERR_CUDA;
+        }
+        x.words = want;
+        x.bank = 0;
+        x.dirty[0] = x.dirty[1] = 0;
+    }
+    if (part_floats > x.part_floats) {
+        if (x.part) cudaFree(x.part);
+        x.part = nullptr;
+        x.part_floats = 0;
+        const size_t want = (part_floats + (size_t(1) << 18) - 1) & ~((size_t(1) << 18) - 1);
+        if (cudaMalloc(&x.part, want * sizeof(float)) != cudaSuccess) {
+            cudaGetLastError();
+            return LA_ERR_NOMEM;
+        }
+        x.part_floats = want;
+    }
+    out->bank = x.bank;
+    out->use = x.base + x.bank * x.words;
+    out->clear = reinterpret_cast<uint32_t*>(x.base + (x.bank ^ 1u) * x.words);
+    out->clear_words = x.dirty[x.bank ^ 1u];
+    out->part = x.part;
+    return LA_OK;
+}
+
+void xch_commit(const XchLease& lease, size_t words_used) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return;
     std::lock_guard<std::mutex> lock(g_ws_mutex);
-    g_ws[dev].bank ^= 1u;
+    XchState& x = g_xch[dev];
+    x.dirty[lease.bank] = words_used;
+    x.dirty[lease.bank ^ 1u] = 0;
+    x.bank = lease.bank ^ 1u;
 }
 
 }  // namespace la
@@ -170,10 +228,14 @@ int la_prefill_ex(const void* q, const void* k, const void* v, const void* g, vo
     const bool use_tc = bf16 && !(flags & LA_FLAG_SIMT) && prefill_tc_supported(B, H, N) == LA_OK;
     if (use_tc) {
         Workspace ws;
-        int rc = workspace_acquire(prefill_tc_workspace_bytes(B, H, N), st, &ws);
+        int rc = workspace_acquire(0, st, &ws);
+        if (rc != LA_OK) return rc;
+        XchLease xl;
+        rc = xch_acquire(prefill_tc_flag_words(B, H, N), prefill_tc_part_floats(B, H, N), st,
+                         &xl);
         if (rc != LA_OK) return rc;
         return launch_prefill_tc(q, k, v, g, out, kv_state_in, kv_state_out, y_debug, B, H, N,
-                                 eps, ws, st);
+                                 eps, ws, xl, st);
     }
     // CUDA-core kernel: y in fp32 (into y_debug when given), then the norm/gate pass.
     float* y = y_debug;

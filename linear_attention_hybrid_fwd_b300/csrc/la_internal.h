@@ -10,30 +10,45 @@ namespace la {
 
 constexpr int kHeadDim = 128;  // the only head size the kernels cover (64 x 128 heads)
 
-// Arrival counters of the tensor-core prefill's cross-head exchange: two banks, one
-// counter per (sequence, chunk).  A launch uses one bank and zeroes the other for the
-// next launch, so no separate reset is needed between calls.
-constexpr int kTcCounterSlots = 1 << 17;
-constexpr size_t kTcCounterBytes = size_t(kTcCounterSlots) * sizeof(unsigned);
 // Per-sequence arrival counters of the decode step (one per sequence b, B <= 65535).
 constexpr int kDecodeCounterSlots = 65536;
 
+// Bit pattern of an exchange slot not yet written: a negative float, which a sum of
+// squares never is.
+constexpr uint32_t kXchEmpty = 0x80808080u;
+
 // Per-device scratch owned by the library (see la_api.cu).
 struct Workspace {
-    void* base = nullptr;      // grown on demand
+    void* base = nullptr;        // grown on demand
     size_t bytes = 0;
-    int* status = nullptr;     // device status word (LA_OK / LA_ERR_TIMEOUT)
-    unsigned* banks = nullptr; // 2 x kTcCounterSlots counters, zeroed at allocation
+    int* status = nullptr;       // device status word (LA_OK / LA_ERR_TIMEOUT)
     unsigned* dec_cnt = nullptr; // kDecodeCounterSlots decode counters, zero between calls
-    unsigned bank = 0;         // the bank the next tensor-core prefill uses
 };
 
 // Returns LA_OK and a workspace of at least `bytes` for the current device.  On the
-// first call for a device the status word and the counter banks are allocated and
+// first call for a device the status word and the decode counters are allocated and
 // zeroed on `st`.
 int workspace_acquire(size_t bytes, cudaStream_t st, Workspace* ws);
-// The tensor-core prefill just launched on the current bank: the next one uses the other.
-void workspace_switch_bank();
+
+// The cross-head exchange of the tensor-core prefill.  Per chunk: the per-token sums of
+// squares of every head half ("partials", written before they are read, never reset)
+// and the chunk's arrival counter and per-token norm factors ("flags"), which live in
+// two banks whose every word holds kXchEmpty until written.  A launch writes one flag
+// bank and resets, in the other, the words that the previous launch wrote there; so
+// every flag bank is all-empty again one launch after its use and nothing runs between
+// calls.
+struct XchLease {
+    float* use = nullptr;        // the flag bank this launch writes (all words empty)
+    uint32_t* clear = nullptr;   // the other flag bank
+    size_t clear_words = 0;      // its words [0, clear_words) to reset to kXchEmpty
+    unsigned bank = 0;
+    float* part = nullptr;       // the partials
+};
+// A lease with at least `flag_words` words per flag bank and `part_floats` partials for
+// the current device.
+int xch_acquire(size_t flag_words, size_t part_floats, cudaStream_t st, XchLease* out);
+// The launch of `lease` was enqueued and will write `words_used` words of its flag bank.
+void xch_commit(const XchLease& lease, size_t words_used);
 
 // Launch accounting behind la_launch_count().
 void note_launches(int n);
@@ -56,9 +71,10 @@ int launch_zero_state(float* S, int64_t n, cudaStream_t st);
 // ---- tensor-core prefill (la_prefill_tc.cu) --------------------------------------
 // Returns LA_ERR_UNSUPPORTED when the shape is outside what the kernel covers.
 int prefill_tc_supported(int B, int H, int64_t N);
-size_t prefill_tc_workspace_bytes(int B, int H, int64_t N);
+size_t prefill_tc_flag_words(int B, int H, int64_t N);
+size_t prefill_tc_part_floats(int B, int H, int64_t N);
 int launch_prefill_tc(const void* q, const void* k, const void* v, const void* g, void* out,
                       const float* S_in, float* S_out, float* y_debug, int B, int H, int64_t N,
-                      float eps, const Workspace& ws, cudaStream_t st);
+                      float eps, const Workspace& ws, const XchLease& xl, cudaStream_t st);
 
 }  // namespace la

@@ -8,7 +8,7 @@
 //     Y_c = Q^_c S_{<c} + (Q^_c K^_c^T * M) V^_c ,    S_{<c+1} = S_{<c} + K^_c^T V^_c
 // with M the inclusive lower-triangular mask and S the fp32 d x d state.
 //
-// Design (one B300 SM per CTA, 212 KiB shared memory, all 512 TMEM columns):
+// Design (one B300 SM per CTA, 209 KiB shared memory, all 512 TMEM columns):
 //  * A cluster of two CTAs owns one head h and runs through every chunk of every
 //    sequence of the batch in order.  The pair splits the d_v columns: CTA r keeps the
 //    state columns S[:, 64r, 64r+64) in TMEM and produces y and out for those columns.
@@ -16,29 +16,32 @@
 //  * The activations are not duplicated: CTA 0 loads q and applies SiLU, CTA 1 does the
 //    same for k, and each bulk-copies its activated 128 x 128 tile into the other's
 //    shared memory.  Each CTA activates its own 64 columns of v.  Both then form the
-//    full score tile Q^ K^T (an MMA, cheap) and their halves of the products.
-//  * Warp roles (28 warps): warp 0 issues TMA loads, warp 1 issues tcgen05 MMAs, warp 2
-//    owns TMEM; warps 4-11 apply SiLU in shared memory and push the activated tile to
-//    the peer; warps 12-15 convert the fp32 state to the bf16 operand of Q^ S and mask
-//    the score tile into the bf16 P operand (written in place over the scores);
-//    warps 16-19 post each chunk's per-token sums of squares; warps 20-23 and 24-27
-//    take alternate chunks and finish them (norm, gate, store).
-//  * The RMSNorm spans all heads of a token.  Per chunk, CTA 1 hands its per-token sums
-//    of squares to CTA 0 through distributed shared memory; CTA 0 writes the head's
-//    sums to a global exchange slot and bumps the slot's counter; a finishing
-//    warpgroup waits (bounded) for all H heads and sums them in a fixed order
-//    (deterministic).  y stays in TMEM (three buffers) while the exchange is in flight,
-//    so its latency is not on the per-chunk path.  All CTAs of the grid must be
-//    co-resident; the host checks that before launching.
-//  * Out tiles leave by TMA store from swizzled staging tiles; q, k, v arrive by TMA in
-//    128B-swizzled tiles, double-buffered.  The score tile is double-buffered in TMEM.
+//    full score tile Q^ K^T (two 128 x 64 halves, cheap MMAs) and their halves of the
+//    products.
+//  * Warp roles of a head's CTA (28 warps): warp 0 issues TMA loads (lane 0: q or k and
+//    v; lane 1: g), warp 1 issues tcgen05 MMAs; warps 4-11 apply SiLU in shared memory
+//    and push the activated tile to the peer; warps 12-15 convert the fp32 state to the
+//    bf16 operand of Q^ S and mask each score half into the bf16 P operand (written in
+//    place over it); warps 16-19 post each chunk's per-token sums of squares; warps
+//    20-23 and 24-27 take alternate chunks and finish them (norm, gate, TMA store).
+//  * The RMSNorm spans all heads of a token.  The SMs the head pairs leave free run
+//    reducer CTAs in the same co-resident grid: each head half posts its 128 per-token
+//    sums of squares to a global slot and counts itself in; a reducer waits (bounded)
+//    for all 2H halves of a chunk, sums them in a fixed order (deterministic) and
+//    publishes the chunk's 128 norm factors, whose slots hold an "empty" bit pattern
+//    until written, so the finishing warps read their factor with one load.  A launch
+//    resets the previous launch's counters and factors in the other of two banks.  y
+//    stays in TMEM (five buffers) while the exchange is in flight.  The host checks
+//    that the whole grid is co-resident before launching.
+//  * q, k, v and g arrive by TMA in 128B-swizzled tiles, double-buffered, with an L2
+//    prefetch a few chunks ahead; out leaves by TMA store from the g tile it replaces.
 //  * SiLU(x) = x/2 (1 + tanh(x/2)) and sigmoid(x) = (1 + tanh(x/2))/2 with the hardware
 //    tanh approximation: one SFU operation per element.
 //  * Every wait is bounded (%globaltimer); a CTA that gives up records LA_ERR_TIMEOUT
 //    in the status word, drains its in-flight copies and MMAs, frees TMEM and exits.
 //
-// TMEM columns: [0,128) scores A0 (P0 over its first 64) | [128,256) A1 (P1) |
-//               [256,320) S (fp32, this CTA's 64 columns) | [320,512) Y0, Y1, Y2.
+// TMEM columns: [0,64) scores half 0 (P over its first 32) | [64,128) half 1 |
+//               [128,192) S (fp32, this CTA's 64 columns) | [192,512) Y0 .. Y4.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -60,11 +63,10 @@ constexpr int D = kHeadDim;
 constexpr int CH = 128;               // tokens per chunk
 constexpr int DV = 64;                // d_v columns per CTA
 constexpr int kThreads = 896;         // 28 warps
-constexpr int kYBufs = 3;
-// CTA 1 posts chunk it only after CTA 0 posted chunk it - kYBufs (through the y ring and
-// the exchange), so kYBufs slots of the pair hand-off never alias.
-constexpr int kPairSlots = kYBufs;
+constexpr int kYBufs = 5;             // y tiles in TMEM
+constexpr int kMaxReducers = 16;      // reducer CTAs (on SMs the head pairs leave free)
 constexpr int kGBufs = 2;             // g tiles in flight (TMA-loaded ahead of the epilogue)
+constexpr int kPrefetch = 4;          // chunks of q, k, v, g prefetched into L2 ahead
 constexpr uint32_t TILE = 32768;      // 128 x 128 bf16 = two swizzled 128 x 64 halves
 constexpr uint32_t HALF = 16384;      // 128 x 64 bf16, one 128B-swizzled block
 constexpr uint32_t OFF_QB = 0;                  // 2 stages: q^ tiles
@@ -74,25 +76,25 @@ constexpr uint32_t OFF_SB = OFF_VB + 2 * HALF;  // bf16 state slice (MN-major B 
 constexpr uint32_t OFF_GB = OFF_SB + HALF;      // kGBufs g tiles (this CTA's 64 columns)
 constexpr uint32_t SMEM_USED = OFF_GB + kGBufs * HALF;  // 208 KiB
 constexpr uint32_t SMEM_DYN = SMEM_USED + 1024; // + alignment slack
-static_assert(SMEM_DYN + sizeof(uint64_t) * 64 + 4096 <= 227 * 1024, "shared memory budget");
-constexpr uint32_t TM_A = 0, TM_S = 256, TM_Y = 320;
+static_assert(SMEM_DYN + 6144 <= 227 * 1024, "shared memory budget");
+constexpr uint32_t TM_A = 0, TM_S = 128, TM_Y = 192;
 constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s
 constexpr uint64_t kDrainNs = 200000000ull;     // 0.2 s
 
-constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, 0, 0);  // A K-major, B K-major
+constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 64, 0, 0);   // A K-major, B K-major
 constexpr uint32_t IDESC_QS = idesc_bf16_f32(128, DV, 0, 1);   // A K-major, B MN-major
 constexpr uint32_t IDESC_KV = idesc_bf16_f32(128, DV, 1, 1);   // A MN-major, B MN-major
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, DV, 0, 1);   // A (TMEM), B MN-major
 
 struct Params {
-    __nv_bfloat16* out;
     const float* S_in;
     float* S_out;
     float* y_dbg;
-    float* xch;          // [B*Nc][CH][H] per-token, per-head sums of squares
-    unsigned* cnt;       // [B*Nc] arrivals of this launch (zero on entry)
-    unsigned* cnt_clear; // the other counter bank, zeroed for the next launch
-    int n_clear;
+    unsigned* cnt;       // [B*Nc] head halves posted, from kXchEmpty
+    float* rn;           // [B*Nc][CH] norm factors (kXchEmpty until written)
+    float* part;         // [B*Nc][2H][CH] per-token sums of squares of each head half
+    uint4* xch_clear;    // the other bank's counters and factors of the previous launch
+    int64_t n_clear4;    // ... as a count of 16-byte words
     int* status;
     int B, H;
     int64_t N;
@@ -102,18 +104,16 @@ struct Params {
 };
 
 struct Shared {
-    uint64_t rawfull[2], xin[2], actdone[2], empty[2];
-    uint64_t afull[2], aempty[2], pfull, sdone, sready;
-    uint64_t yfull[kYBufs], yempty[kYBufs], gfull[kGBufs], gempty[kGBufs];
-    uint64_t ssown[kPairSlots], ssx[kPairSlots], mmadone;
+    uint64_t rawqk[2], rawv[2], xin[2], actdone[2], qkempty[2], vempty[2];
+    uint64_t afull[2], aempty[2], pfull[2], sdone, sready;
+    uint64_t yfull[kYBufs], yempty[kYBufs], gfull[kGBufs], gempty[kGBufs], mmadone;
     uint32_t tmem_base;
     int abort_flag;
     int verdict[5];  // group-uniform wait results (SiLU, mask, post, finish 0, finish 1)
-    int issued;      // iterations whose loads the producer issued
+    int issued;      // iterations whose q or k loads the producer issued
     int xin_seen;    // iterations whose peer tile the MMA issuer consumed
     int g_issued;    // iterations whose g tile was issued
-    float own[kPairSlots][CH];  // this CTA's per-token sums of squares (CTA 0 only)
-    float xs[kPairSlots][CH];   // CTA 1's per-token sums of squares (received by CTA 0)
+    float red[2][CH];  // reducer: per-token sums over the heads, one row per d_v half
 };
 
 // ------------------------------------------------------------------ numerics
@@ -228,29 +228,63 @@ __device__ __forceinline__ void store_row_bf16(uint8_t* blk, int r, int part,
     }
 }
 
-// ------------------------------------------------------------------ the kernel
-// Bounded spin until *cnt >= target; false (after raising the abort) on timeout or when
-// the CTA is aborting.
-__device__ bool spin_counter(Shared& sh, int* status, const unsigned* cnt, unsigned target) {
+// Bounded spin until *cnt == target (unsigned compare); false after a timeout (raising
+// the abort) or when the CTA is aborting.
+__device__ bool spin_until(Shared& sh, int* status, const unsigned* cnt, unsigned target) {
     uint64_t t0 = 0;
-    for (uint32_t k = 0;; ++k) {
-        if (ld_acquire_gpu(cnt) >= target) return true;
-        if ((k & 63u) == 63u) {
-            if (abort_set(sh)) return false;
-            const uint64_t now = global_timer_ns();
-            if (t0 == 0) t0 = now;
-            else if (now - t0 > kTimeoutNs) {
-                raise_abort(sh, status);
-                return false;
-            }
+    for (;;) {
+        if (ld_acquire_gpu(cnt) == target) return true;
+        if (abort_set(sh)) return false;
+        const uint64_t now = global_timer_ns();
+        if (t0 == 0) {
+            t0 = now;
+        } else if (now - t0 > kTimeoutNs) {
+            raise_abort(sh, status);
+            return false;
         }
+        __nanosleep(200);
     }
 }
 
+// Reducer CTA: for its chunks (every R-th), waits for all 2H head halves' per-token sums
+// of squares, adds them in a fixed order (per d_v half over the heads in order, then
+// the two halves) and publishes r_t = 1 / sqrt(mean + eps) for the chunk's 128 tokens.
+__device__ void reducer(Shared& sh, const Params& p, int j, int R) {
+    const int tid = threadIdx.x;
+    if (tid >= 2 * CH) return;
+    const int t = tid & (CH - 1), r = tid >> 7;
+    const bool leader = tid == 0;
+    const int H = p.H, total = p.B * p.Nc;
+    const unsigned target = kXchEmpty + 2u * static_cast<unsigned>(H);
+    for (int it = j; it < total; it += R) {
+        if (leader) sh.verdict[0] = spin_until(sh, p.status, p.cnt + it, target) ? 1 : 0;
+        named_bar_sync(1, 2 * CH);
+        if (!*reinterpret_cast<volatile int*>(&sh.verdict[0])) break;
+        const float* src = p.part + (static_cast<size_t>(it) * 2 * H + r) * CH + t;
+        float acc = 0.f;
+        for (int h0 = 0; h0 < H; h0 += 32) {
+            float v[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+                v[k] = h0 + k < H ? __ldcg(src + static_cast<size_t>(2 * (h0 + k)) * CH) : 0.f;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) acc += v[k];
+        }
+        sh.red[r][t] = acc;
+        named_bar_sync(1, 2 * CH);
+        if (r == 0) {
+            const float tot = sh.red[0][t] + sh.red[1][t];
+            __stcg(p.rn + static_cast<size_t>(it) * CH + t, rsqrtf(tot * p.inv_width + p.eps));
+        }
+        named_bar_sync(1, 2 * CH);  // sh.red is rewritten by the next chunk
+    }
+}
+
+// ------------------------------------------------------------------ the kernel
 __global__ void __launch_bounds__(kThreads, 1)
     k_prefill_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
-                 const Params p) {
+                 const __grid_constant__ CUtensorMap to, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ Shared sh;
     uint8_t* sm = reinterpret_cast<uint8_t*>(
@@ -265,18 +299,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int col0 = h * D + static_cast<int>(rank) * DV;    // first feature column owned
     const uint32_t own_off = rank == 0 ? OFF_QB : OFF_KB;    // the tile this CTA activates
 
-    // the other counter bank is zeroed here for the next launch
-    for (int i = blockIdx.x * kThreads + tid; i < p.n_clear; i += gridDim.x * kThreads)
-        p.cnt_clear[i] = 0u;
+    // the previous launch's counters and factors in the other bank become empty again
+    {
+        const uint4 e = make_uint4(kXchEmpty, kXchEmpty, kXchEmpty, kXchEmpty);
+        for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + tid; i < p.n_clear4;
+             i += static_cast<int64_t>(gridDim.x) * kThreads)
+            p.xch_clear[i] = e;
+    }
+    if (static_cast<int>(blockIdx.x) >= 2 * H) {  // a reducer CTA (no TMEM, no cluster traffic)
+        if (tid == 0) {
+            sh.abort_flag = 0;
+            sh.verdict[0] = 0;
+        }
+        __syncthreads();
+        reducer(sh, p, static_cast<int>(blockIdx.x) - 2 * H, static_cast<int>(gridDim.x) - 2 * H);
+        return;
+    }
 
     if (tid == 0) {
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&sh.rawfull[s], 1);
+            mbar_init(&sh.rawqk[s], 1);
+            mbar_init(&sh.rawv[s], 1);
             mbar_init(&sh.xin[s], 1);
             mbar_init(&sh.actdone[s], 1);
-            mbar_init(&sh.empty[s], 2);  // this CTA's MMAs and the peer's
+            mbar_init(&sh.qkempty[s], 2);  // this CTA's MMAs and the peer's
+            mbar_init(&sh.vempty[s], 1);
             mbar_init(&sh.afull[s], 1);
             mbar_init(&sh.aempty[s], 1);
+            mbar_init(&sh.pfull[s], 1);
         }
         for (int y = 0; y < kYBufs; ++y) {
             mbar_init(&sh.yfull[y], 1);
@@ -286,11 +336,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.gfull[i], 1);
             mbar_init(&sh.gempty[i], 1);
         }
-        for (int i = 0; i < kPairSlots; ++i) {
-            mbar_init(&sh.ssown[i], CH);  // this CTA's post warps, one arrival per row
-            mbar_init(&sh.ssx[i], CH);    // one remote arrival per token row of CTA 1
-        }
-        mbar_init(&sh.pfull, 1);
         mbar_init(&sh.sdone, 1);
         mbar_init(&sh.sready, 1);
         mbar_init(&sh.mmadone, 1);
@@ -312,33 +357,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // -------------------------------------------- TMA producer: q or k, and v
             const CUtensorMap* own_map = rank == 0 ? &tq : &tk;
+            for (int j = 0; j < kPrefetch && j < total; ++j) {
+                const int bj = j / Nc, cj = j - bj * Nc;
+                tma_prefetch_3d(own_map, h * D, cj * CH, bj);
+                tma_prefetch_3d(own_map, h * D + 64, cj * CH, bj);
+                tma_prefetch_3d(&tv, col0, cj * CH, bj);
+            }
             int issued = 0;
             for (int it = 0; it < total; ++it) {
                 const int b = it / Nc, c = it - b * Nc;
                 const int s = it & 1;
                 const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
-                if (!wait_bar(sh, p.status, &sh.empty[s], ph ^ 1u)) break;
+                if (it + kPrefetch < total) {
+                    const int jp = it + kPrefetch, bj = jp / Nc, cj = jp - bj * Nc;
+                    tma_prefetch_3d(own_map, h * D, cj * CH, bj);
+                    tma_prefetch_3d(own_map, h * D + 64, cj * CH, bj);
+                    tma_prefetch_3d(&tv, col0, cj * CH, bj);
+                }
+                if (!wait_bar(sh, p.status, &sh.qkempty[s], ph ^ 1u)) break;
                 uint8_t* own = sm + own_off + s * TILE;
-                uint8_t* vt = sm + OFF_VB + s * HALF;
-                mbar_arrive_expect_tx(&sh.rawfull[s], TILE + HALF);
-                tma_load_3d(own, own_map, h * D, c * CH, b, &sh.rawfull[s]);
-                tma_load_3d(own + HALF, own_map, h * D + 64, c * CH, b, &sh.rawfull[s]);
-                tma_load_3d(vt, &tv, col0, c * CH, b, &sh.rawfull[s]);
+                mbar_arrive_expect_tx(&sh.rawqk[s], TILE);
+                tma_load_3d(own, own_map, h * D, c * CH, b, &sh.rawqk[s]);
+                tma_load_3d(own + HALF, own_map, h * D + 64, c * CH, b, &sh.rawqk[s]);
                 mbar_arrive_expect_tx(&sh.xin[s], TILE);  // the peer's activated tile
                 issued = it + 1;
+                if (!wait_bar(sh, p.status, &sh.vempty[s], ph ^ 1u)) break;
+                mbar_arrive_expect_tx(&sh.rawv[s], HALF);
+                tma_load_3d(sm + OFF_VB + s * HALF, &tv, col0, c * CH, b, &sh.rawv[s]);
             }
             sh.issued = issued;
             // drain: the last loads land before this CTA may exit
-            for (int it = issued - 2 < 0 ? 0 : issued - 2; it < issued; ++it)
-                wait_bar(sh, p.status, &sh.rawfull[it & 1],
-                         static_cast<uint32_t>(it >> 1) & 1u, false, kDrainNs);
+            for (int it = issued - 2 < 0 ? 0 : issued - 2; it < issued; ++it) {
+                const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
+                wait_bar(sh, p.status, &sh.rawqk[it & 1], ph, false, kDrainNs);
+                wait_bar(sh, p.status, &sh.rawv[it & 1], ph, false, kDrainNs);
+            }
         } else if (lane == 1) {
             // -------------------------------------------- TMA producer: g
+            for (int j = 0; j < kPrefetch && j < total; ++j)
+                tma_prefetch_3d(&tg, col0, (j % Nc) * CH, j / Nc);
             int issued = 0;
             for (int it = 0; it < total; ++it) {
                 const int b = it / Nc, c = it - b * Nc;
                 const int gs = it % kGBufs;
                 const uint32_t gph = static_cast<uint32_t>(it / kGBufs) & 1u;
+                if (it + kPrefetch < total) {
+                    const int jp = it + kPrefetch;
+                    tma_prefetch_3d(&tg, col0, (jp % Nc) * CH, jp / Nc);
+                }
                 if (!wait_bar(sh, p.status, &sh.gempty[gs], gph ^ 1u)) break;
                 mbar_arrive_expect_tx(&sh.gfull[gs], HALF);
                 tma_load_3d(sm + OFF_GB + gs * HALF, &tg, col0, c * CH, b, &sh.gfull[gs]);
@@ -359,16 +425,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait_bar(sh, p.status, &sh.actdone[s], ph)) break;
                 if (!wait_bar(sh, p.status, &sh.xin[s], ph)) break;
                 seen = it + 1;
-                if (!wait_bar(sh, p.status, &sh.aempty[s], ph ^ 1u)) break;
-                tc_fence_after();
                 const uint32_t qa = sbase + OFF_QB + s * TILE, ka = sbase + OFF_KB + s * TILE;
                 const uint32_t va = sbase + OFF_VB + s * HALF, sb = sbase + OFF_SB;
-                const uint32_t tA = tm + TM_A + s * 128, tY = tm + TM_Y + yb * DV;
-                // scores A = Q^ K^T (128 x 128)
+                const uint32_t tY = tm + TM_Y + yb * DV;
+                bool ok = true;
+                // scores, in two halves of 64 key tokens: A_j = Q^ K^_j^T (128 x 64)
+                for (int j = 0; j < 2 && ok; ++j) {
+                    if (!wait_bar(sh, p.status, &sh.aempty[j], par ^ 1u)) { ok = false; break; }
+                    tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_ss(tA, desc_kmajor(qa, ks), desc_kmajor(ka, ks), IDESC_QK, ks > 0);
-                mma_commit(&sh.afull[s]);
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_ss(tm + TM_A + 64 * j, desc_kmajor(qa, ks),
+                               desc_kmajor(ka + 8192 * j, ks), IDESC_QK, ks > 0);
+                    mma_commit(&sh.afull[j]);
+                }
+                if (!ok) break;
                 if (!wait_bar(sh, p.status, &sh.yempty[yb], yph ^ 1u)) break;
                 if (!wait_bar(sh, p.status, &sh.sready, par)) break;
                 tc_fence_after();
@@ -381,61 +452,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int ks = 0; ks < 8; ++ks)
                     mma_ss(tm + TM_S, desc_mnmajor(ka, ks), desc_mnmajor(va, ks), IDESC_KV, 1u);
                 mma_commit(&sh.sdone);
-                if (!wait_bar(sh, p.status, &sh.pfull, par)) break;
-                tc_fence_after();
-                // Y += P V^, P = mask(A) in bf16 over the first 64 columns of A
+                // q^ and k^ of this stage are no longer read (this CTA and the peer's copy)
+                mma_commit_multicast(&sh.qkempty[s], static_cast<uint16_t>(3u));
+                // Y += P_j V^_j, P_j = mask(A_j) in bf16 over the first 32 columns of A_j
+                for (int j = 0; j < 2 && ok; ++j) {
+                    if (!wait_bar(sh, p.status, &sh.pfull[j], par)) { ok = false; break; }
+                    tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_ts(tY, tA + ks * 8, desc_mnmajor(va, ks), IDESC_PV, 1u);
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_ts(tY, tm + TM_A + 64 * j + ks * 8,
+                               desc_mnmajor(va + 8192 * j, ks), IDESC_PV, 1u);
+                    mma_commit(&sh.aempty[j]);
+                }
+                if (!ok) break;
                 mma_commit(&sh.yfull[yb]);
-                mma_commit(&sh.aempty[s]);
-                mma_commit_multicast(&sh.empty[s], static_cast<uint16_t>(3u));
+                mma_commit(&sh.vempty[s]);
             }
             sh.xin_seen = seen;
             mma_commit(&sh.mmadone);
             wait_bar(sh, p.status, &sh.mmadone, 0, false, kDrainNs);
         }
-    } else if (warp == 2 || warp == 3) {
-        // ------------------------------------------------ publishers (CTA 0): the head's
-        // per-token sums of squares into the exchange slot, then the slot's counter.
-        // Warps 2 and 3 take alternate chunks.
-        if (rank == 0) {
-            for (int it = warp - 2; it < total; it += 2) {
-                const int xslot = it % kPairSlots;
-                const uint32_t xph = static_cast<uint32_t>(it / kPairSlots) & 1u;
-                int ok = 1;
-                if (lane == 0)
-                    ok = wait_bar(sh, p.status, &sh.ssown[xslot], xph) &&
-                         wait_bar<true>(sh, p.status, &sh.ssx[xslot], xph);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-                while (!mbar_try_wait(&sh.ssown[xslot], xph)) {
-                }
-                while (!mbar_try_wait_acq_cluster(&sh.ssx[xslot], xph)) {
-                }
-                float* dst = p.xch + static_cast<size_t>(it) * CH * H + h;
-#pragma unroll
-                for (int k = 0; k < CH / 32; ++k) {
-                    const int t = lane + 32 * k;
-                    dst[static_cast<size_t>(t) * H] = sh.own[xslot][t] + sh.xs[xslot][t];
-                }
-                __syncwarp();
-                if (lane == 0) red_release_gpu_add(p.cnt + it, 1u);
-            }
-        }
     } else if (warp >= 4 && warp < 12) {
-        // ------------------------------------------------ SiLU (two warpgroups)
+        // ------------------------------------------------ SiLU (two warpgroups): the own
+        // tile first (then pushed to the peer), then this CTA's v columns
         const int t = (tid - 128) & 127;   // tile row (token)
-        const int part = (tid - 128) >> 7; // 0: own-tile half 0 + v chunks 0-3; 1: the rest
+        const int part = (tid - 128) >> 7; // own-tile half; v chunks 4 part .. 4 part + 3
         const bool leader = tid == 128;
         const uint32_t peer_own = map_to_rank(sbase + own_off, peer);
         const uint32_t peer_xin = map_to_rank(smem_addr(&sh.xin[0]), peer);
         for (int it = 0; it < total; ++it) {
             const int s = it & 1;
             const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
-            if (!group_wait(sh, p.status, &sh.rawfull[s], ph, leader, 1, 256, 0)) break;
+            if (!group_wait(sh, p.status, &sh.rawqk[s], ph, leader, 1, 256, 0)) break;
             uint8_t* blk = sm + own_off + s * TILE + part * HALF;
-            uint8_t* vt = sm + OFF_VB + s * HALF;
             uint4 x[4];
 #pragma unroll
             for (int g4 = 0; g4 < 2; ++g4) {
@@ -446,6 +495,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < 4; ++j)
                     *reinterpret_cast<uint4*>(blk + swz(t, 4 * g4 + j)) = silu_chunk(x[j]);
             }
+            fence_proxy_async_smem();
+            named_bar_sync(1, 256);
+            if (leader)
+                bulk_copy_to_peer(peer_own + s * TILE, sbase + own_off + s * TILE, TILE,
+                                  peer_xin + s * 8);
+            if (!group_wait(sh, p.status, &sh.rawv[s], ph, leader, 1, 256, 0)) break;
+            uint8_t* vt = sm + OFF_VB + s * HALF;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 x[j] = *reinterpret_cast<const uint4*>(vt + swz(t, 4 * part + j));
@@ -454,11 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4*>(vt + swz(t, 4 * part + j)) = silu_chunk(x[j]);
             fence_proxy_async_smem();
             named_bar_sync(1, 256);
-            if (leader) {
-                mbar_arrive(&sh.actdone[s]);
-                bulk_copy_to_peer(peer_own + s * TILE, sbase + own_off + s * TILE, TILE,
-                                  peer_xin + s * 8);
-            }
+            if (leader) mbar_arrive(&sh.actdone[s]);
         }
     } else if (warp >= 12 && warp < 16) {
         // ------------------------------------------------ state conversion + mask
@@ -525,47 +577,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             named_bar_sync(2, 128);
             if (leader) mbar_arrive(&sh.sready);
-            // (2) P = A masked to s <= t, bf16, written over the first 64 columns of A
-            const int a = it & 1;
-            const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
-            if (!group_wait(sh, p.status, &sh.afull[a], ph, leader, 2, 128, 1)) break;
-            tc_fence_after();
-            const uint32_t tA = lb + TM_A + a * 128;
-#pragma unroll
-            for (int part = 0; part < 4; ++part) {
-                uint32_t pk[16];
-                if (32 * part <= q4 * 32 + 31) {  // some lane of this warp has s <= t here
-                    uint32_t r[32];
-                    LA_TMEM_LD32(tA + 32 * part, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int s0 = 32 * part + 2 * j;
-                        const float lo = s0 <= t ? __uint_as_float(r[2 * j]) : 0.f;
-                        const float hi = s0 + 1 <= t ? __uint_as_float(r[2 * j + 1]) : 0.f;
-                        pk[j] = pack_bf16x2(lo, hi);
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) pk[j] = 0u;
+            // (2) P_j = A_j masked to s <= t, bf16, over the first 32 columns of A_j
+            bool ok = true;
+            for (int j = 0; j < 2; ++j) {
+                if (!group_wait(sh, p.status, &sh.afull[j], static_cast<uint32_t>(it) & 1u,
+                                leader, 2, 128, 1)) {
+                    ok = false;
+                    break;
                 }
-                // columns [16 part, 16 part + 16) of A were read in an earlier or this part
-                LA_TMEM_ST16(tA + 16 * part, pk);
+                tc_fence_after();
+                const uint32_t tA = lb + TM_A + 64 * j;
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    const int sb0 = 64 * j + 32 * part;  // first key token of these columns
+                    uint32_t pk[16];
+                    if (sb0 <= q4 * 32 + 31) {  // some lane of this warp has s <= t here
+                        uint32_t r[32];
+                        LA_TMEM_LD32(tA + 32 * part, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int s0 = sb0 + 2 * jj;
+                            const float lo = s0 <= t ? __uint_as_float(r[2 * jj]) : 0.f;
+                            const float hi = s0 + 1 <= t ? __uint_as_float(r[2 * jj + 1]) : 0.f;
+                            pk[jj] = pack_bf16x2(lo, hi);
+                        }
+                    } else {
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) pk[jj] = 0u;
+                    }
+                    // columns [16 part, 16 part + 16) of A_j were read in this or an earlier part
+                    LA_TMEM_ST16(tA + 16 * part, pk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                named_bar_sync(2, 128);
+                if (leader) mbar_arrive(&sh.pfull[j]);
             }
-            tmem_wait_st();
-            tc_fence_before();
-            named_bar_sync(2, 128);
-            if (leader) mbar_arrive(&sh.pfull);
+            if (!ok) break;
         }
     } else if (warp >= 16 && warp < 20) {
-        // ------------------------------------------------ post: per-token sums of squares
-        // into this CTA's slot (CTA 0) or into CTA 0's peer slot (CTA 1)
+        // ------------------------------------------------ post: this head half's per-token
+        // sums of squares into the chunk's slot, then the chunk's counter
         const int q4 = warp & 3;
         const int t = q4 * 32 + lane;  // token row
         const bool leader = t == 0;
         const uint32_t lb = tm + (static_cast<uint32_t>(q4 * 32) << 16);
-        const uint32_t peer_xs = map_to_rank(smem_addr(&sh.xs[0][0]), peer);
-        const uint32_t peer_ssx = map_to_rank(smem_addr(&sh.ssx[0]), peer);
         for (int it = 0; it < total; ++it) {
             const int yb = it % kYBufs;
             const uint32_t yph = static_cast<uint32_t>(it / kYBufs) & 1u;
@@ -581,14 +638,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < 32; ++j)
                     ss = fmaf(__uint_as_float(y[j]), __uint_as_float(y[j]), ss);
             }
-            const int xslot = it % kPairSlots;
-            if (rank == 1) {
-                st_cluster_f32(peer_xs + static_cast<uint32_t>((xslot * CH + t) * 4), ss);
-                mbar_arrive_remote(peer_ssx + xslot * 8);
-            } else {
-                sh.own[xslot][t] = ss;
-                mbar_arrive(&sh.ssown[xslot]);
-            }
+            __stcg(p.part + (static_cast<size_t>(it) * 2 * H + 2 * h + rank) * CH + t, ss);
+            named_bar_sync(3, 128);
+            if (leader) red_release_gpu_add(p.cnt + it, 1u);  // orders the group's stores
         }
     } else if (warp >= 20) {
         // ------------------------------------------------ finish: norm, gate, store
@@ -605,52 +657,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t yph = static_cast<uint32_t>(it / kYBufs) & 1u;
             const int gs = it % kGBufs;
             const uint32_t gph = static_cast<uint32_t>(it / kGBufs) & 1u;
-            const int64_t tok = static_cast<int64_t>(c) * CH + t;
-            const bool valid = tok < p.N;
-            const size_t grow = (static_cast<size_t>(b) * p.N + tok) * H * D + col0;
-            // every head has posted this chunk (bounded wait on the counter)
-            if (leader) sh.verdict[slot] = spin_counter(sh, p.status, p.cnt + it, H) ? 1 : 0;
-            named_bar_sync(bar_id, 128);
-            if (!*reinterpret_cast<volatile int*>(&sh.verdict[slot])) break;
-            // r_t from the H head sums of token t, in head order (one batch of loads)
-            float acc = 0.f;
+            // r_t, published by the chunk's reducer (re-read, bounded, until written)
+            float rn = 0.f;
+            bool ready = false;
             {
-                const float* src = p.xch + (static_cast<size_t>(it) * CH + t) * H;
-                if (H == 64) {
-                    const float4* s4 = reinterpret_cast<const float4*>(src);
-                    float4 v[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] = __ldcg(s4 + j);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) acc += ((v[j].x + v[j].y) + (v[j].z + v[j].w));
-                } else if ((H & 3) == 0) {
-                    const float4* s4 = reinterpret_cast<const float4*>(src);
-                    const int n4 = H >> 2;
-                    for (int base = 0; base < n4; base += 8) {
-                        float4 v[8];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            v[j] = base + j < n4 ? __ldcg(s4 + base + j)
-                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) acc += ((v[j].x + v[j].y) + (v[j].z + v[j].w));
+                const float* src = p.rn + static_cast<size_t>(it) * CH + t;
+                uint64_t t0 = 0;
+                for (;;) {
+                    rn = __ldcg(src);
+                    if (__float_as_uint(rn) != kXchEmpty) {
+                        ready = true;
+                        break;
                     }
-                } else {
-                    for (int base = 0; base < H; base += 16) {
-                        float v[16];
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) v[j] = base + j < H ? __ldcg(src + base + j) : 0.f;
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) acc += v[j];
+                    if (abort_set(sh)) break;
+                    const uint64_t now = global_timer_ns();
+                    if (t0 == 0) {
+                        t0 = now;
+                    } else if (now - t0 > kTimeoutNs) {
+                        raise_abort(sh, p.status);
+                        break;
                     }
+                    __nanosleep(200);
                 }
             }
-            const float rn = rsqrtf(acc * p.inv_width + p.eps);
-            // out = y (fp32, TMEM) * r_t * sigmoid(g) (g from the TMA-loaded tile)
+            if (!named_bar_and(bar_id, 128, ready)) break;
+            // out = y (fp32, TMEM) * r_t * sigmoid(g), written over the g tile, then stored
             if (!group_wait(sh, p.status, &sh.gfull[gs], gph, leader, bar_id, 128, slot)) break;
             if (!group_wait(sh, p.status, &sh.yfull[yb], yph, leader, bar_id, 128, slot)) break;
             tc_fence_after();
-            const uint8_t* gt = sm + OFF_GB + gs * HALF;
+            uint8_t* gt = sm + OFF_GB + gs * HALF;
+            const int64_t tok = static_cast<int64_t>(c) * CH + t;
+            const bool valid = tok < p.N;
+            const size_t grow = (static_cast<size_t>(b) * p.N + tok) * H * D + col0;
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
                 uint32_t y[32];
@@ -666,7 +704,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint4 gv = *reinterpret_cast<const uint4*>(gt + swz(t, 4 * part + j));
+                    uint4* gp = reinterpret_cast<uint4*>(gt + swz(t, 4 * part + j));
+                    const uint4 gv = *gp;
                     const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
                     uint32_t w[4];
 #pragma unroll
@@ -676,18 +715,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         w[k2] = pack_bf16x2(y0 * sigmoid_t(bf_lo(gw[k2])),
                                             y1 * sigmoid_t(bf_hi(gw[k2])));
                     }
-                    if (valid)
-                        reinterpret_cast<uint4*>(p.out + grow)[4 * part + j] =
-                            make_uint4(w[0], w[1], w[2], w[3]);
+                    *gp = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
             tc_fence_before();
+            fence_proxy_async_smem();
             named_bar_sync(bar_id, 128);
             if (leader) {
                 mbar_arrive(&sh.yempty[yb]);
+                tma_store_3d(&to, gt, col0, c * CH, b);  // rows past N are dropped
+                bulk_commit_group();
+                bulk_wait_group_read0();  // the tile may take the next g once read
                 mbar_arrive(&sh.gempty[gs]);
             }
         }
+        if (leader) bulk_wait_group0();
     }
 
     // ---------------------------------------------------- teardown
@@ -773,41 +815,59 @@ int max_active_clusters() {
     return g_max_clusters[dev];
 }
 
+// Flag bank layout for one launch: [counters, padded to 4][norm factors].
+size_t flag_cnt_words(int B, int64_t N) {
+    const size_t units = static_cast<size_t>(B) * ((N + CH - 1) / CH);
+    return (units + 3) & ~size_t(3);
+}
+
+int reducers_for(int H) {
+    const int spare = max_active_clusters() - H;
+    const int clusters = spare < kMaxReducers / 2 ? spare : kMaxReducers / 2;
+    return clusters > 0 ? 2 * clusters : 0;
+}
+
 }  // namespace
 
 int prefill_tc_supported(int B, int H, int64_t N) {
     if (N <= 0 || N > (int64_t(1) << 30)) return LA_ERR_UNSUPPORTED;
     const int64_t Nc = (N + CH - 1) / CH;
-    if (static_cast<int64_t>(B) * Nc > kTcCounterSlots) return LA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(B) * Nc > (int64_t(1) << 30) / CH) return LA_ERR_UNSUPPORTED;
     if (!encoder()) return LA_ERR_UNSUPPORTED;
-    const int mc = max_active_clusters();
-    // every head's pair must be resident at once for the cross-head exchange
-    if (mc <= 0 || H > mc) return LA_ERR_UNSUPPORTED;
+    // every head's pair and at least one reducer pair must be resident at once
+    if (max_active_clusters() <= 0 || reducers_for(H) <= 0) return LA_ERR_UNSUPPORTED;
     return LA_OK;
 }
 
-size_t prefill_tc_workspace_bytes(int B, int H, int64_t N) {
-    const int64_t Nc = (N + CH - 1) / CH;
-    return static_cast<size_t>(B) * Nc * CH * H * sizeof(float);
+size_t prefill_tc_flag_words(int B, int H, int64_t N) {
+    (void)H;
+    return flag_cnt_words(B, N) + static_cast<size_t>(B) * ((N + CH - 1) / CH) * CH;
+}
+
+size_t prefill_tc_part_floats(int B, int H, int64_t N) {
+    return static_cast<size_t>(B) * ((N + CH - 1) / CH) * 2 * H * CH;
 }
 
 int launch_prefill_tc(const void* q, const void* k, const void* v, const void* g, void* out,
                       const float* S_in, float* S_out, float* y_debug, int B, int H, int64_t N,
-                      float eps, const Workspace& ws, cudaStream_t st) {
+                      float eps, const Workspace& ws, const XchLease& xl, cudaStream_t st) {
     const int64_t Nc = (N + CH - 1) / CH;
-    CUtensorMap mq, mk, mv, mg;
+    const int R = reducers_for(H);
+    if (R <= 0) return LA_ERR_UNSUPPORTED;
+    CUtensorMap mq, mk, mv, mg, mo;
     if (!encode_io_map(&mq, q, B, H, N) || !encode_io_map(&mk, k, B, H, N) ||
-        !encode_io_map(&mv, v, B, H, N) || !encode_io_map(&mg, g, B, H, N))
+        !encode_io_map(&mv, v, B, H, N) || !encode_io_map(&mg, g, B, H, N) ||
+        !encode_io_map(&mo, out, B, H, N))
         return LA_ERR_UNSUPPORTED;
     Params prm;
-    prm.out = static_cast<__nv_bfloat16*>(out);
     prm.S_in = S_in;
     prm.S_out = S_out;
     prm.y_dbg = y_debug;
-    prm.xch = static_cast<float*>(ws.base);
-    prm.cnt = ws.banks + (ws.bank & 1u) * kTcCounterSlots;
-    prm.cnt_clear = ws.banks + ((ws.bank & 1u) ^ 1u) * kTcCounterSlots;
-    prm.n_clear = kTcCounterSlots;
+    prm.cnt = reinterpret_cast<unsigned*>(xl.use);
+    prm.rn = xl.use + flag_cnt_words(B, N);
+    prm.part = xl.part;
+    prm.xch_clear = reinterpret_cast<uint4*>(xl.clear);
+    prm.n_clear4 = static_cast<int64_t>(xl.clear_words / 4);
     prm.status = ws.status;
     prm.B = B;
     prm.H = H;
@@ -816,7 +876,7 @@ int launch_prefill_tc(const void* q, const void* k, const void* v, const void* g
     prm.eps = eps;
     prm.inv_width = 1.0f / static_cast<float>(H * D);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * H), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * H + R), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = SMEM_DYN;
     cfg.stream = st;
@@ -827,11 +887,11 @@ int launch_prefill_tc(const void* q, const void* k, const void* v, const void* g
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, k_prefill_tc, mq, mk, mv, mg, prm) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, k_prefill_tc, mq, mk, mv, mg, mo, prm) != cudaSuccess) {
         cudaGetLastError();
         return LA_ERR_CUDA;
     }
-    workspace_switch_bank();
+    xch_commit(xl, prefill_tc_flag_words(B, H, N));
     note_launches(1);
     return LA_OK;
 }
