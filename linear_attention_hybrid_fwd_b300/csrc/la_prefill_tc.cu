@@ -33,8 +33,9 @@
 //    resets the previous launch's counters and factors in the other of two banks.  y
 //    stays in TMEM (five buffers) while the exchange is in flight.  The host checks
 //    that the whole grid is co-resident before launching.
-//  * q, k, v and g arrive by TMA in 128B-swizzled tiles, double-buffered, with an L2
-//    prefetch a few chunks ahead; out leaves by TMA store from the g tile it replaces.
+//  * q, k, v and g arrive by TMA in 128B-swizzled tiles, double-buffered (an L2
+//    prefetch ahead of them is wired in but set to zero chunks: it bought nothing on
+//    B300); out leaves by TMA store from the g tile it replaces.
 //  * SiLU(x) = x/2 (1 + tanh(x/2)) and sigmoid(x) = (1 + tanh(x/2))/2 with the hardware
 //    tanh approximation: one SFU operation per element.
 //  * Every wait is bounded (%globaltimer); a CTA that gives up records LA_ERR_TIMEOUT
@@ -66,7 +67,7 @@ constexpr int kThreads = 896;         // 28 warps
 constexpr int kYBufs = 5;             // y tiles in TMEM
 constexpr int kMaxReducers = 16;      // reducer CTAs (on SMs the head pairs leave free)
 constexpr int kGBufs = 2;             // g tiles in flight (TMA-loaded ahead of the epilogue)
-constexpr int kPrefetch = 4;          // chunks of q, k, v, g prefetched into L2 ahead
+constexpr int kPrefetch = 0;          // chunks of q, k, v, g prefetched into L2 ahead (off: no gain measured)
 constexpr uint32_t TILE = 32768;      // 128 x 128 bf16 = two swizzled 128 x 64 halves
 constexpr uint32_t HALF = 16384;      // 128 x 64 bf16, one 128B-swizzled block
 constexpr uint32_t OFF_QB = 0;                  // 2 stages: q^ tiles
