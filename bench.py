@@ -350,8 +350,8 @@ def run_ours(a):
     flops = 4.0 * w.B * w.H * w.N * w.d * w.d
     tflops = flops / (ms / 1e3) / 1e12
     io_bytes = 5.0 * w.B * w.N * w.H * w.d * 2 + w.B * w.H * w.d * w.d * 4
-    # the dominant kernel is the whole step on the tensor-core path (one kernel
-    # after a small counter reset); its duration is the per-step event time
+    # the dominant kernel is the whole step on the tensor-core path (one launch per
+    # step); its duration is the per-step event time
     kern = "la_prefill_simt" if a.simt else "la_prefill_tc"
     src = [os.path.join(ROOT, "linear_attention_hybrid_fwd_b300", "csrc", f)
            for f in ("la_simt.cu",) if a.simt] or [

@@ -99,6 +99,35 @@ int la_prefill_ex(const void* q, const void* k, const void* v, const void* g, vo
                   int H, int64_t N, int d, int dtype, float eps, unsigned flags,
                   void* cuda_stream);
 
+/*
+ * Packed ("varlen") prefill of num_seqs sequences of different lengths, stored back to
+ * back without padding -- the padding optimisation the MiniMax-01 deep dive lists
+ * among its training-infrastructure improvements ("Post Training and Infra"), for the
+ * same layer ("Hybrid Modeling", mechanism steps 2-4).  Each sequence is its own
+ * causal recurrence (its own state, starting from kv_state_in[b] or zeros); the
+ * RMSNorm is per token as in la_prefill.
+ *   cu_seqlens   HOST array of num_seqs + 1 int64 token offsets: cu_seqlens[0] = 0,
+ *                non-decreasing; sequence b is tokens [cu_seqlens[b], cu_seqlens[b+1])
+ *                (empty sequences are allowed).  T = cu_seqlens[num_seqs].
+ *   q, k, v, g   in  [T][H][d] (dtype);  out  out [T][H][d]
+ *   kv_state_out out [num_seqs][H][d][d] fp32 or NULL (may equal kv_state_in)
+ *   kv_state_in  in  [num_seqs][H][d][d] fp32 or NULL (zeros)
+ *   y_debug      out [T][H][d] fp32 pre-norm y, or NULL
+ * The chunk table is uploaded from host memory on the stream, which waits for the
+ * stream's earlier work first.  Errors as for la_prefill_ex; additionally
+ * LA_ERR_INVALID_ARG for a cu_seqlens that does not start at 0 or decreases.
+ */
+int la_prefill_varlen_ex(const void* q, const void* k, const void* v, const void* g, void* out,
+                         float* kv_state_out, const float* kv_state_in, float* y_debug,
+                         const int64_t* cu_seqlens, int num_seqs, int H, int d, int dtype,
+                         float eps, unsigned flags, void* cuda_stream);
+
+/* la_prefill_varlen_ex with bf16 I/O, zero initial states, no y_debug, eps = 1e-6 and
+   the legacy default stream. */
+int la_prefill_varlen(const void* q, const void* k, const void* v, const void* g, void* out,
+                      float* kv_state_out, const int64_t* cu_seqlens, int num_seqs, int H,
+                      int d);
+
 /* Extended decode step: as la_decode_step with dtype, eps, an optional fp32 pre-norm
    y_debug [B][H][d] (or NULL) and a stream. */
 int la_decode_step_ex(float* kv_state, const void* q, const void* k, const void* v,
@@ -107,10 +136,10 @@ int la_decode_step_ex(float* kv_state, const void* q, const void* k, const void*
 
 /* Which prefill kernel la_prefill_ex would run for this shape on the current device:
    0 = tensor-core kernel, 1 = CUDA-core kernel, or -(la_status) if the arguments are
-   invalid.  The tensor-core kernel covers bf16, d = 128, H no larger than the number
+   invalid.  The tensor-core kernel covers bf16, d = 128, H smaller than the number
    of two-CTA clusters the device holds at once (it keeps every head resident for the
-   cross-head RMSNorm and runs the B sequences one after another), N <= 2^30 and
-   B * ceil(N / 128) <= 131072. */
+   cross-head RMSNorm, runs the B sequences one after another, and needs at least one
+   more cluster for the norm's reducers), N <= 2^30 and B * ceil(N / 128) <= 131072. */
 int la_prefill_path(int B, int H, int64_t N, int d, int dtype, unsigned flags);
 
 /*

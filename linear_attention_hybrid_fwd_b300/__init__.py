@@ -9,6 +9,7 @@ or no CUDA device is present, the calls raise.
 Functions carry the C names:
 
 * ``la_prefill(q, k, v, g, ...)``       -- prefill of ``[B, N, H, d]`` inputs
+* ``la_prefill_varlen(q, k, v, g, cu_seqlens, ...)`` -- packed sequences of any lengths
 * ``la_decode_step(kv_state, q, ...)``  -- one token per sequence, ``[B, H, d]`` inputs
 * ``la_decode_step_noalloc``           -- the same step with the library's fixed scratch,
                                           for callers that cannot let it allocate
@@ -20,7 +21,7 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["la_prefill", "la_decode_step", "la_decode_step_noalloc", "la_status_string", "la_get_device_status",
+__all__ = ["la_prefill", "la_prefill_varlen", "la_decode_step", "la_decode_step_noalloc", "la_status_string", "la_get_device_status",
            "la_version", "la_launch_count", "la_prefill_path", "LaError", "library_path",
            "load_library", "LA_BF16", "LA_F32", "LA_FLAG_SIMT"]
 
@@ -61,6 +62,12 @@ def load_library():
     lib.la_prefill_ex.argtypes = [vp, vp, vp, vp, vp, fp, fp, fp, i32, i32, i64, i32, i32, f32,
                                   u32, vp]
     lib.la_prefill_ex.restype = i32
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    lib.la_prefill_varlen_ex.argtypes = [vp, vp, vp, vp, vp, fp, fp, fp, i64p, i32, i32, i32, i32,
+                                         f32, u32, vp]
+    lib.la_prefill_varlen_ex.restype = i32
+    lib.la_prefill_varlen.argtypes = [vp, vp, vp, vp, vp, fp, i64p, i32, i32, i32]
+    lib.la_prefill_varlen.restype = i32
     lib.la_decode_step.argtypes = [fp, vp, vp, vp, vp, vp, i32, i32, i32]
     lib.la_decode_step.restype = i32
     lib.la_decode_step_ex.argtypes = [fp, vp, vp, vp, vp, vp, fp, i32, i32, i32, i32, f32, vp]
@@ -170,6 +177,46 @@ def la_prefill(q, k, v, g, out=None, kv_state_out=None, kv_state_in=None, y_debu
         _stream_handle(stream))
     if rc != LA_OK:
         raise LaError(rc, "la_prefill")
+    return out, kv_state_out
+
+
+def la_prefill_varlen(q, k, v, g, cu_seqlens, out=None, kv_state_out=None, kv_state_in=None,
+                      y_debug=None, eps: float = 1e-6, simt: bool = False, want_state: bool = True,
+                      stream=None):
+    """Packed prefill: ``q, k, v, g`` are ``[T, H, d]`` (bf16 or fp32, contiguous, CUDA),
+    sequence ``b`` is rows ``cu_seqlens[b]:cu_seqlens[b+1]`` (``cu_seqlens``: host ints,
+    ``num_seqs + 1`` of them, starting at 0).  Returns ``(out, kv_state_out)`` with
+    ``kv_state_out`` ``[num_seqs, H, d, d]`` fp32."""
+    import torch
+    T, H, d = q.shape
+    cu = [int(x) for x in (cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist")
+                           else cu_seqlens)]
+    S = len(cu) - 1
+    if S < 1:
+        raise ValueError("cu_seqlens needs at least two entries")
+    if cu[-1] != T:
+        raise ValueError(f"cu_seqlens ends at {cu[-1]}, q has {T} tokens")
+    if out is None:
+        out = torch.empty_like(q)
+    if kv_state_out is None and want_state:
+        kv_state_out = torch.empty((S, H, d, d), device=q.device, dtype=torch.float32)
+    _check([q, k, v, g, out, kv_state_out, kv_state_in, y_debug],
+           ["q", "k", "v", "g", "out", "kv_state_out", "kv_state_in", "y_debug"])
+    for t, n in ((k, "k"), (v, "v"), (g, "g"), (out, "out")):
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{n} must match q in shape and dtype")
+    for t, n in ((kv_state_out, "kv_state_out"), (kv_state_in, "kv_state_in")):
+        if t is not None and (tuple(t.shape) != (S, H, d, d) or t.dtype != torch.float32):
+            raise ValueError(f"{n} must be float32 [num_seqs, H, d, d]")
+    if y_debug is not None and (y_debug.shape != q.shape or y_debug.dtype != torch.float32):
+        raise ValueError("y_debug must be float32 [T, H, d]")
+    cu_arr = (ctypes.c_int64 * (S + 1))(*cu)
+    rc = load_library().la_prefill_varlen_ex(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out), _ptr(kv_state_out), _ptr(kv_state_in),
+        _ptr(y_debug), cu_arr, S, H, d, _dtype_code(q), float(eps), LA_FLAG_SIMT if simt else 0,
+        _stream_handle(stream))
+    if rc != LA_OK:
+        raise LaError(rc, "la_prefill_varlen")
     return out, kv_state_out
 
 

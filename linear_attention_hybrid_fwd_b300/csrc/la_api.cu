@@ -8,6 +8,7 @@
 
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "../../include/lightning_attn.h"
 #include "la_internal.h"
@@ -30,6 +31,12 @@ struct XchState {
 };
 XchState g_xch[kMaxDevices];
 
+struct ItemBuf {
+    int4* dev = nullptr;     // chunk table of the last packed-batch launch
+    size_t cap = 0;
+};
+ItemBuf g_items[kMaxDevices];
+
 struct WorkspaceReaper {
     ~WorkspaceReaper() {
         // Process teardown: the driver may already be gone; ignore errors.
@@ -37,6 +44,8 @@ struct WorkspaceReaper {
             if (x.base) cudaFree(x.base);
             if (x.part) cudaFree(x.part);
         }
+        for (auto& i : g_items)
+            if (i.dev) cudaFree(i.dev);
         for (auto& w : g_ws) {
             if (w.base) cudaFree(w.base);
             if (w.status) cudaFree(w.status);
@@ -156,6 +165,31 @@ void xch_commit(const XchLease& lease, size_t words_used) {
     x.bank = lease.bank ^ 1u;
 }
 
+// Uploads a packed batch's chunk table into the device's table buffer (grown on demand)
+// on `st`.  The copy is from pageable memory, so it waits for the stream's earlier work.
+int items_upload(const std::vector<int4>& items, cudaStream_t st, const int4** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    ItemBuf& b = g_items[dev];
+    if (items.size() > b.cap) {
+        if (b.dev) cudaFree(b.dev);
+        b.dev = nullptr;
+        b.cap = 0;
+        const size_t want = (items.size() + 4095) & ~size_t(4095);
+        if (cudaMalloc(&b.dev, want * sizeof(int4)) != cudaSuccess) {
+            cudaGetLastError();
+            return LA_ERR_NOMEM;
+        }
+        b.cap = want;
+    }
+    if (cudaMemcpyAsync(b.dev, items.data(), items.size() * sizeof(int4), cudaMemcpyHostToDevice,
+                        st) != cudaSuccess)
+        return LA_ERR_CUDA;
+    *out = b.dev;
+    return LA_OK;
+}
+
 }  // namespace la
 
 using namespace la;
@@ -231,8 +265,8 @@ int la_prefill_ex(const void* q, const void* k, const void* v, const void* g, vo
         int rc = workspace_acquire(0, st, &ws);
         if (rc != LA_OK) return rc;
         XchLease xl;
-        rc = xch_acquire(prefill_tc_flag_words(B, H, N), prefill_tc_part_floats(B, H, N), st,
-                         &xl);
+        const int items = prefill_tc_items(B, N);
+        rc = xch_acquire(prefill_tc_flag_words(items), prefill_tc_part_floats(items, H), st, &xl);
         if (rc != LA_OK) return rc;
         return launch_prefill_tc(q, k, v, g, out, kv_state_in, kv_state_out, y_debug, B, H, N,
                                  eps, ws, xl, st);
@@ -264,6 +298,109 @@ int la_prefill(const void* q, const void* k, const void* v, const void* g, void*
                float* kv_state_out, int B, int H, int64_t N, int d) {
     return la_prefill_ex(q, k, v, g, out, kv_state_out, nullptr, nullptr, B, H, N, d, LA_BF16,
                          1e-6f, 0u, nullptr);
+}
+
+int la_prefill_varlen_ex(const void* q, const void* k, const void* v, const void* g, void* out,
+                         float* kv_state_out, const float* kv_state_in, float* y_debug,
+                         const int64_t* cu_seqlens, int num_seqs, int H, int d, int dtype,
+                         float eps, unsigned flags, void* cuda_stream) {
+    // ---- host-side validation: nothing is launched or written on failure ----
+    if (num_seqs <= 0 || H <= 0 || d <= 0 || !cu_seqlens) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_BF16 && dtype != LA_F32) return LA_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f) || !isfinite(eps)) return LA_ERR_INVALID_ARG;
+    if (flags & ~LA_FLAG_SIMT) return LA_ERR_INVALID_ARG;
+    if (d != kHeadDim) return LA_ERR_UNSUPPORTED;
+    if (num_seqs > 65535 || H > 4096) return LA_ERR_UNSUPPORTED;
+    if (cu_seqlens[0] != 0) return LA_ERR_INVALID_ARG;
+    for (int b = 0; b < num_seqs; ++b)
+        if (cu_seqlens[b + 1] < cu_seqlens[b]) return LA_ERR_INVALID_ARG;
+    const int64_t T = cu_seqlens[num_seqs];
+    if (T > (int64_t(1) << 30) / H) return LA_ERR_INVALID_ARG;
+    const bool bf16 = dtype == LA_BF16;
+    const size_t esz = bf16 ? 2 : 4;
+    const size_t io_bytes = (size_t)T * H * d * esz;
+    const size_t state_bytes = (size_t)num_seqs * H * d * d * sizeof(float);
+    if (T > 0 && (!q || !k || !v || !g || !out)) return LA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, g, out, kv_state_out, kv_state_in, y_debug};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return LA_ERR_MISALIGNED;
+    if (T > 0) {
+        const void* ins[] = {q, k, v, g};
+        for (const void* p : ins)
+            if (overlaps(out, io_bytes, p, io_bytes)) return LA_ERR_INVALID_ARG;
+        if (overlaps(kv_state_out, state_bytes, out, io_bytes)) return LA_ERR_INVALID_ARG;
+        if (y_debug && overlaps(y_debug, (size_t)T * H * d * 4, out, io_bytes))
+            return LA_ERR_INVALID_ARG;
+    }
+    if (kv_state_in && kv_state_out && kv_state_in != kv_state_out &&
+        overlaps(kv_state_in, state_bytes, kv_state_out, state_bytes))
+        return LA_ERR_INVALID_ARG;
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
+    const size_t head_state = (size_t)H * d * d;  // floats per sequence
+    // sequences without tokens: their final state is their initial state
+    if (kv_state_out && kv_state_out != kv_state_in) {
+        for (int b = 0; b < num_seqs; ++b) {
+            if (cu_seqlens[b + 1] != cu_seqlens[b]) continue;
+            int rc = kv_state_in ? cuda_status(cudaMemcpyAsync(
+                                       kv_state_out + b * head_state, kv_state_in + b * head_state,
+                                       head_state * sizeof(float), cudaMemcpyDeviceToDevice, st))
+                                 : launch_zero_state(kv_state_out + b * head_state,
+                                                     (int64_t)head_state, st);
+            if (rc != LA_OK) return rc;
+        }
+    }
+    if (T == 0) return LA_OK;
+
+    const bool use_tc =
+        bf16 && !(flags & LA_FLAG_SIMT) && prefill_tc_supported(1, H, T) == LA_OK;
+    if (use_tc) {
+        std::vector<int4> items;
+        for (int b = 0; b < num_seqs; ++b) {
+            const int64_t n = cu_seqlens[b + 1] - cu_seqlens[b];
+            for (int64_t c0 = 0; c0 < n; c0 += kTcChunk) {
+                const int64_t nv = n - c0 < kTcChunk ? n - c0 : kTcChunk;
+                items.push_back(make_int4(static_cast<int>(cu_seqlens[b] + c0),
+                                          static_cast<int>(nv), b, c0 == 0 ? 1 : 0));
+            }
+        }
+        Workspace ws;
+        int rc = workspace_acquire(0, st, &ws);
+        if (rc != LA_OK) return rc;
+        const int total = static_cast<int>(items.size());
+        XchLease xl;
+        rc = xch_acquire(prefill_tc_flag_words(total), prefill_tc_part_floats(total, H), st, &xl);
+        if (rc != LA_OK) return rc;
+        const int4* dev_items = nullptr;
+        rc = items_upload(items, st, &dev_items);
+        if (rc != LA_OK) return rc;
+        return launch_prefill_tc_varlen(q, k, v, g, out, kv_state_in, kv_state_out, y_debug, H,
+                                        T, total, dev_items, eps, ws, xl, st);
+    }
+    // CUDA-core kernel (fp32 I/O, or on request): one prefill per sequence
+    const size_t row = (size_t)H * d;  // elements per token
+    for (int b = 0; b < num_seqs; ++b) {
+        const int64_t r0 = cu_seqlens[b], n = cu_seqlens[b + 1] - r0;
+        if (n == 0) continue;
+        const size_t off = (size_t)r0 * row * esz;
+        auto at = [&](const void* p) {
+            return static_cast<const void*>(static_cast<const char*>(p) + off);
+        };
+        int rc = la_prefill_ex(at(q), at(k), at(v), at(g), static_cast<char*>(out) + off,
+                               kv_state_out ? kv_state_out + b * head_state : nullptr,
+                               kv_state_in ? kv_state_in + b * head_state : nullptr,
+                               y_debug ? y_debug + (size_t)r0 * row : nullptr, 1, H, n, d, dtype,
+                               eps, flags, cuda_stream);
+        if (rc != LA_OK) return rc;
+    }
+    return LA_OK;
+}
+
+int la_prefill_varlen(const void* q, const void* k, const void* v, const void* g, void* out,
+                      float* kv_state_out, const int64_t* cu_seqlens, int num_seqs, int H,
+                      int d) {
+    return la_prefill_varlen_ex(q, k, v, g, out, kv_state_out, nullptr, nullptr, cu_seqlens,
+                                num_seqs, H, d, LA_BF16, 1e-6f, 0u, nullptr);
 }
 
 int la_decode_step_ex(float* kv_state, const void* q, const void* k, const void* v,

@@ -71,10 +71,20 @@ int launch_zero_state(float* S, int64_t n, cudaStream_t st);
 // ---- tensor-core prefill (la_prefill_tc.cu) --------------------------------------
 // Returns LA_ERR_UNSUPPORTED when the shape is outside what the kernel covers.
 int prefill_tc_supported(int B, int H, int64_t N);
-size_t prefill_tc_flag_words(int B, int H, int64_t N);
-size_t prefill_tc_part_floats(int B, int H, int64_t N);
+// (sequence, chunk) items of a batch of B sequences of N tokens
+int prefill_tc_items(int B, int64_t N);
+size_t prefill_tc_flag_words(int items);
+size_t prefill_tc_part_floats(int items, int H);
 int launch_prefill_tc(const void* q, const void* k, const void* v, const void* g, void* out,
                       const float* S_in, float* S_out, float* y_debug, int B, int H, int64_t N,
                       float eps, const Workspace& ws, const XchLease& xl, cudaStream_t st);
+// A packed batch of T tokens: items (device, `total` of them) = {first row, valid rows,
+// sequence, first chunk of its sequence}, chunks of 128 tokens in order.
+int launch_prefill_tc_varlen(const void* q, const void* k, const void* v, const void* g,
+                             void* out, const float* S_in, float* S_out, float* y_debug, int H,
+                             int64_t T, int total, const int4* items, float eps,
+                             const Workspace& ws, const XchLease& xl, cudaStream_t st);
+// Chunk length of the tensor-core prefill (the items' granularity).
+constexpr int kTcChunk = 128;
 
 }  // namespace la

@@ -33,9 +33,12 @@
 //    resets the previous launch's counters and factors in the other of two banks.  y
 //    stays in TMEM (five buffers) while the exchange is in flight.  The host checks
 //    that the whole grid is co-resident before launching.
-//  * q, k, v and g arrive by TMA in 128B-swizzled tiles, double-buffered (an L2
-//    prefetch ahead of them is wired in but set to zero chunks: it bought nothing on
-//    B300); out leaves by TMA store from the g tile it replaces.
+//  * q, k, v and g arrive by TMA in 128B-swizzled tiles, double-buffered; out leaves by
+//    TMA store from the g tile it replaces (row by row for a partial chunk of a packed
+//    batch, whose last rows belong to the next sequence).
+//  * A batch is a list of (sequence, chunk) items run in order: B sequences of N tokens,
+//    or sequences of any lengths packed back to back (the rows of a chunk past its
+//    sequence's end are zeroed after loading, so they add nothing to any product).
 //  * SiLU(x) = x/2 (1 + tanh(x/2)) and sigmoid(x) = (1 + tanh(x/2))/2 with the hardware
 //    tanh approximation: one SFU operation per element.
 //  * Every wait is bounded (%globaltimer); a CTA that gives up records LA_ERR_TIMEOUT
@@ -67,7 +70,6 @@ constexpr int kThreads = 896;         // 28 warps
 constexpr int kYBufs = 5;             // y tiles in TMEM
 constexpr int kMaxReducers = 16;      // reducer CTAs (on SMs the head pairs leave free)
 constexpr int kGBufs = 2;             // g tiles in flight (TMA-loaded ahead of the epilogue)
-constexpr int kPrefetch = 0;          // chunks of q, k, v, g prefetched into L2 ahead (off: no gain measured)
 constexpr uint32_t TILE = 32768;      // 128 x 128 bf16 = two swizzled 128 x 64 halves
 constexpr uint32_t HALF = 16384;      // 128 x 64 bf16, one 128B-swizzled block
 constexpr uint32_t OFF_QB = 0;                  // 2 stages: q^ tiles
@@ -88,6 +90,7 @@ constexpr uint32_t IDESC_KV = idesc_bf16_f32(128, DV, 1, 1);   // A MN-major, B 
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, DV, 0, 1);   // A (TMEM), B MN-major
 
 struct Params {
+    __nv_bfloat16* out;  // partial chunks of packed batches are stored from here
     const float* S_in;
     float* S_out;
     float* y_dbg;
@@ -97,12 +100,42 @@ struct Params {
     uint4* xch_clear;    // the other bank's counters and factors of the previous launch
     int64_t n_clear4;    // ... as a count of 16-byte words
     int* status;
+    const int4* items;   // per iteration {first row, valid rows, sequence, first chunk of it}
+                         // (packed varlen batches), or nullptr: B sequences of N tokens
     int B, H;
-    int64_t N;
-    int Nc;
+    int64_t N;           // tokens per sequence (the packed token count for varlen)
+    int Nc;              // chunks per sequence (uniform batches)
+    int total;           // iterations: (sequence, chunk) items in order
     float eps;
     float inv_width;     // 1 / (H * d)
 };
+
+// One (sequence, chunk) iteration: its tile rows start at token y of slab z of the
+// [z][token][feature] tensor maps; rows >= nvalid are not part of the sequence.
+struct Item {
+    int y, z, nvalid, b, first;
+};
+template <bool kVarlen>
+__device__ __forceinline__ Item item_at(const Params& p, int it) {
+    Item r;
+    if constexpr (kVarlen) {
+        const int4 e = p.items[it];
+        r.y = e.x;
+        r.z = 0;
+        r.nvalid = e.y;
+        r.b = e.z;
+        r.first = e.w;
+    } else {
+        const int b = it / p.Nc, c = it - b * p.Nc;
+        const int64_t rem = p.N - static_cast<int64_t>(c) * CH;
+        r.y = c * CH;
+        r.z = b;
+        r.nvalid = rem < CH ? static_cast<int>(rem) : CH;
+        r.b = b;
+        r.first = c == 0;
+    }
+    return r;
+}
 
 struct Shared {
     uint64_t rawqk[2], rawv[2], xin[2], actdone[2], qkempty[2], vempty[2];
@@ -255,7 +288,7 @@ __device__ void reducer(Shared& sh, const Params& p, int j, int R) {
     if (tid >= 2 * CH) return;
     const int t = tid & (CH - 1), r = tid >> 7;
     const bool leader = tid == 0;
-    const int H = p.H, total = p.B * p.Nc;
+    const int H = p.H, total = p.total;
     const unsigned target = kXchEmpty + 2u * static_cast<unsigned>(H);
     for (int it = j; it < total; it += R) {
         if (leader) sh.verdict[0] = spin_until(sh, p.status, p.cnt + it, target) ? 1 : 0;
@@ -282,6 +315,10 @@ __device__ void reducer(Shared& sh, const Params& p, int j, int R) {
 }
 
 // ------------------------------------------------------------------ the kernel
+// kVarlen: the items come from the packed batch's table (p.items) rather than from the
+// uniform B x ceil(N / 128) grid of chunks; the uniform instance carries none of the
+// packed batch's checks.
+template <bool kVarlen>
 __global__ void __launch_bounds__(kThreads, 1)
     k_prefill_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
@@ -295,8 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t rank = cluster_ctarank();
     const uint32_t peer = rank ^ 1u;
     const int h = blockIdx.x >> 1;
-    const int H = p.H, Nc = p.Nc;
-    const int total = p.B * Nc;                              // (sequence, chunk) iterations
+    const int H = p.H;
+    const int total = p.total;                               // (sequence, chunk) iterations
     const int col0 = h * D + static_cast<int>(rank) * DV;    // first feature column owned
     const uint32_t own_off = rank == 0 ? OFF_QB : OFF_KB;    // the tile this CTA activates
 
@@ -358,33 +395,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // -------------------------------------------- TMA producer: q or k, and v
             const CUtensorMap* own_map = rank == 0 ? &tq : &tk;
-            for (int j = 0; j < kPrefetch && j < total; ++j) {
-                const int bj = j / Nc, cj = j - bj * Nc;
-                tma_prefetch_3d(own_map, h * D, cj * CH, bj);
-                tma_prefetch_3d(own_map, h * D + 64, cj * CH, bj);
-                tma_prefetch_3d(&tv, col0, cj * CH, bj);
-            }
             int issued = 0;
             for (int it = 0; it < total; ++it) {
-                const int b = it / Nc, c = it - b * Nc;
+                const Item im = item_at<kVarlen>(p, it);
                 const int s = it & 1;
                 const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
-                if (it + kPrefetch < total) {
-                    const int jp = it + kPrefetch, bj = jp / Nc, cj = jp - bj * Nc;
-                    tma_prefetch_3d(own_map, h * D, cj * CH, bj);
-                    tma_prefetch_3d(own_map, h * D + 64, cj * CH, bj);
-                    tma_prefetch_3d(&tv, col0, cj * CH, bj);
-                }
                 if (!wait_bar(sh, p.status, &sh.qkempty[s], ph ^ 1u)) break;
                 uint8_t* own = sm + own_off + s * TILE;
                 mbar_arrive_expect_tx(&sh.rawqk[s], TILE);
-                tma_load_3d(own, own_map, h * D, c * CH, b, &sh.rawqk[s]);
-                tma_load_3d(own + HALF, own_map, h * D + 64, c * CH, b, &sh.rawqk[s]);
+                tma_load_3d(own, own_map, h * D, im.y, im.z, &sh.rawqk[s]);
+                tma_load_3d(own + HALF, own_map, h * D + 64, im.y, im.z, &sh.rawqk[s]);
                 mbar_arrive_expect_tx(&sh.xin[s], TILE);  // the peer's activated tile
                 issued = it + 1;
                 if (!wait_bar(sh, p.status, &sh.vempty[s], ph ^ 1u)) break;
                 mbar_arrive_expect_tx(&sh.rawv[s], HALF);
-                tma_load_3d(sm + OFF_VB + s * HALF, &tv, col0, c * CH, b, &sh.rawv[s]);
+                tma_load_3d(sm + OFF_VB + s * HALF, &tv, col0, im.y, im.z, &sh.rawv[s]);
             }
             sh.issued = issued;
             // drain: the last loads land before this CTA may exit
@@ -395,20 +420,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         } else if (lane == 1) {
             // -------------------------------------------- TMA producer: g
-            for (int j = 0; j < kPrefetch && j < total; ++j)
-                tma_prefetch_3d(&tg, col0, (j % Nc) * CH, j / Nc);
             int issued = 0;
             for (int it = 0; it < total; ++it) {
-                const int b = it / Nc, c = it - b * Nc;
+                const Item im = item_at<kVarlen>(p, it);
                 const int gs = it % kGBufs;
                 const uint32_t gph = static_cast<uint32_t>(it / kGBufs) & 1u;
-                if (it + kPrefetch < total) {
-                    const int jp = it + kPrefetch;
-                    tma_prefetch_3d(&tg, col0, (jp % Nc) * CH, jp / Nc);
-                }
                 if (!wait_bar(sh, p.status, &sh.gempty[gs], gph ^ 1u)) break;
                 mbar_arrive_expect_tx(&sh.gfull[gs], HALF);
-                tma_load_3d(sm + OFF_GB + gs * HALF, &tg, col0, c * CH, b, &sh.gfull[gs]);
+                tma_load_3d(sm + OFF_GB + gs * HALF, &tg, col0, im.y, im.z, &sh.gfull[gs]);
                 issued = it + 1;
             }
             sh.g_issued = issued;
@@ -485,16 +504,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = it & 1;
             const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
             if (!group_wait(sh, p.status, &sh.rawqk[s], ph, leader, 1, 256, 0)) break;
+            // rows past a packed sequence's end hold the next sequence's tokens and become
+            // zero; in a uniform batch the rows past N are already the tensor map's zero
+            // fill, and SiLU(0) = 0
+            const bool live = !kVarlen || t < p.items[it].y;
             uint8_t* blk = sm + own_off + s * TILE + part * HALF;
             uint4 x[4];
+            if (live) {
 #pragma unroll
-            for (int g4 = 0; g4 < 2; ++g4) {
+                for (int g4 = 0; g4 < 2; ++g4) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    x[j] = *reinterpret_cast<const uint4*>(blk + swz(t, 4 * g4 + j));
+                    for (int j = 0; j < 4; ++j)
+                        x[j] = *reinterpret_cast<const uint4*>(blk + swz(t, 4 * g4 + j));
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint4*>(blk + swz(t, 4 * g4 + j)) = silu_chunk(x[j]);
+                    for (int j = 0; j < 4; ++j)
+                        *reinterpret_cast<uint4*>(blk + swz(t, 4 * g4 + j)) = silu_chunk(x[j]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<uint4*>(blk + swz(t, j)) = make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
             named_bar_sync(1, 256);
@@ -503,12 +532,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   peer_xin + s * 8);
             if (!group_wait(sh, p.status, &sh.rawv[s], ph, leader, 1, 256, 0)) break;
             uint8_t* vt = sm + OFF_VB + s * HALF;
+            if (live) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                x[j] = *reinterpret_cast<const uint4*>(vt + swz(t, 4 * part + j));
+                for (int j = 0; j < 4; ++j)
+                    x[j] = *reinterpret_cast<const uint4*>(vt + swz(t, 4 * part + j));
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                *reinterpret_cast<uint4*>(vt + swz(t, 4 * part + j)) = silu_chunk(x[j]);
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4*>(vt + swz(t, 4 * part + j)) = silu_chunk(x[j]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4*>(vt + swz(t, 4 * part + j)) =
+                        make_uint4(0u, 0u, 0u, 0u);
+            }
             fence_proxy_async_smem();
             named_bar_sync(1, 256);
             if (leader) mbar_arrive(&sh.actdone[s]);
@@ -521,7 +557,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lb = tm + (static_cast<uint32_t>(q4 * 32) << 16);
         uint8_t* sbk = sm + OFF_SB;
         for (int it = 0; it <= total; ++it) {
-            const int b = it / Nc, c = it - b * Nc;
+            const Item im = item_at<kVarlen>(p, it < total ? it : total - 1);
+            const bool first = it == total || im.first;  // a sequence ends before it
             // (1) the bf16 operand S_{<c} for iteration it
             if (it > 0) {
                 if (!group_wait(sh, p.status, &sh.sdone, static_cast<uint32_t>(it - 1) & 1u,
@@ -529,9 +566,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 tc_fence_after();
             }
-            if (c == 0) {
+            if (first) {
                 if (it > 0 && p.S_out) {  // the finished sequence's final state
-                    float* dst = p.S_out + ((static_cast<size_t>(b - 1) * H + h) * D + t) * D +
+                    const int pb = item_at<kVarlen>(p, it - 1).b;
+                    float* dst = p.S_out + ((static_cast<size_t>(pb) * H + h) * D + t) * D +
                                  rank * DV;
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
@@ -547,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (it == total) break;
                 const float* src =
-                    p.S_in ? p.S_in + ((static_cast<size_t>(b) * H + h) * D + t) * D + rank * DV
+                    p.S_in ? p.S_in + ((static_cast<size_t>(im.b) * H + h) * D + t) * D + rank * DV
                            : nullptr;
 #pragma unroll
                 for (int part = 0; part < 2; ++part) {
@@ -653,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int slot = 3 + fg;
         const uint32_t lb = tm + (static_cast<uint32_t>(q4 * 32) << 16);
         for (int it = fg; it < total; it += 2) {
-            const int b = it / Nc, c = it - b * Nc;
+            const Item im = item_at<kVarlen>(p, it);
             const int yb = it % kYBufs;
             const uint32_t yph = static_cast<uint32_t>(it / kYBufs) & 1u;
             const int gs = it % kGBufs;
@@ -687,9 +725,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!group_wait(sh, p.status, &sh.yfull[yb], yph, leader, bar_id, 128, slot)) break;
             tc_fence_after();
             uint8_t* gt = sm + OFF_GB + gs * HALF;
-            const int64_t tok = static_cast<int64_t>(c) * CH + t;
-            const bool valid = tok < p.N;
-            const size_t grow = (static_cast<size_t>(b) * p.N + tok) * H * D + col0;
+            const bool valid = t < im.nvalid;
+            const size_t grow =
+                (static_cast<size_t>(im.z) * p.N + static_cast<size_t>(im.y) + t) * H * D + col0;
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
                 uint32_t y[32];
@@ -720,11 +758,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tc_fence_before();
+            if (kVarlen && im.nvalid < CH) {
+                // a partial chunk of a packed batch: its last rows are the next sequence's,
+                // so only this sequence's rows are stored, row by row
+                named_bar_sync(bar_id, 128);
+                if (valid) {
+                    uint4* orow = reinterpret_cast<uint4*>(p.out + grow);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        orow[j] = *reinterpret_cast<const uint4*>(gt + swz(t, j));
+                }
+                named_bar_sync(bar_id, 128);
+                if (leader) {
+                    mbar_arrive(&sh.yempty[yb]);
+                    mbar_arrive(&sh.gempty[gs]);
+                }
+                continue;
+            }
             fence_proxy_async_smem();
             named_bar_sync(bar_id, 128);
             if (leader) {
                 mbar_arrive(&sh.yempty[yb]);
-                tma_store_3d(&to, gt, col0, c * CH, b);  // rows past N are dropped
+                tma_store_3d(&to, gt, col0, im.y, im.z);  // rows past N are dropped
                 bulk_commit_group();
                 bulk_wait_group_read0();  // the tile may take the next g once read
                 mbar_arrive(&sh.gempty[gs]);
@@ -795,7 +850,9 @@ int max_active_clusters() {
     std::lock_guard<std::mutex> lock(g_occ_mutex);
     if (g_max_clusters[dev] != 0) return g_max_clusters[dev];
     int n = -1;
-    if (cudaFuncSetAttribute(k_prefill_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(k_prefill_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(SMEM_DYN)) == cudaSuccess &&
+        cudaFuncSetAttribute(k_prefill_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_DYN)) == cudaSuccess) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2, 1, 1);
@@ -809,17 +866,20 @@ int max_active_clusters() {
         cfg.attrs = at;
         cfg.numAttrs = 1;
         int m = 0;
-        if (cudaOccupancyMaxActiveClusters(&m, k_prefill_tc, &cfg) == cudaSuccess) n = m;
+        int m1 = 0;
+        if (cudaOccupancyMaxActiveClusters(&m, k_prefill_tc<false>, &cfg) == cudaSuccess &&
+            cudaOccupancyMaxActiveClusters(&m1, k_prefill_tc<true>, &cfg) == cudaSuccess)
+            n = m < m1 ? m : m1;
     }
     cudaGetLastError();
     g_max_clusters[dev] = n > 0 ? n : -1;
     return g_max_clusters[dev];
 }
 
-// Flag bank layout for one launch: [counters, padded to 4][norm factors].
-size_t flag_cnt_words(int B, int64_t N) {
-    const size_t units = static_cast<size_t>(B) * ((N + CH - 1) / CH);
-    return (units + 3) & ~size_t(3);
+// Flag bank layout for one launch of `total` items: [counters, padded to 4][factors].
+size_t flag_cnt_words(int total) { return (static_cast<size_t>(total) + 3) & ~size_t(3); }
+size_t flag_words_for(int total) {
+    return flag_cnt_words(total) + static_cast<size_t>(total) * CH;
 }
 
 int reducers_for(int H) {
@@ -840,19 +900,24 @@ int prefill_tc_supported(int B, int H, int64_t N) {
     return LA_OK;
 }
 
-size_t prefill_tc_flag_words(int B, int H, int64_t N) {
-    (void)H;
-    return flag_cnt_words(B, N) + static_cast<size_t>(B) * ((N + CH - 1) / CH) * CH;
+size_t prefill_tc_flag_words(int items) { return flag_words_for(items); }
+
+size_t prefill_tc_part_floats(int items, int H) {
+    return static_cast<size_t>(items) * 2 * H * CH;
 }
 
-size_t prefill_tc_part_floats(int B, int H, int64_t N) {
-    return static_cast<size_t>(B) * ((N + CH - 1) / CH) * 2 * H * CH;
+int prefill_tc_items(int B, int64_t N) {
+    return static_cast<int>(static_cast<int64_t>(B) * ((N + CH - 1) / CH));
 }
 
-int launch_prefill_tc(const void* q, const void* k, const void* v, const void* g, void* out,
-                      const float* S_in, float* S_out, float* y_debug, int B, int H, int64_t N,
-                      float eps, const Workspace& ws, const XchLease& xl, cudaStream_t st) {
-    const int64_t Nc = (N + CH - 1) / CH;
+namespace {
+
+// Launches the kernel over `total` items: B sequences of N tokens (items == nullptr) or
+// a packed batch viewed as one slab of N tokens (items: the per-item table on device).
+int launch_items(const void* q, const void* k, const void* v, const void* g, void* out,
+                 const float* S_in, float* S_out, float* y_debug, int B, int H, int64_t N,
+                 int total, const int4* items, float eps, const Workspace& ws,
+                 const XchLease& xl, cudaStream_t st) {
     const int R = reducers_for(H);
     if (R <= 0) return LA_ERR_UNSUPPORTED;
     CUtensorMap mq, mk, mv, mg, mo;
@@ -861,19 +926,22 @@ int launch_prefill_tc(const void* q, const void* k, const void* v, const void* g
         !encode_io_map(&mo, out, B, H, N))
         return LA_ERR_UNSUPPORTED;
     Params prm;
+    prm.out = static_cast<__nv_bfloat16*>(out);
     prm.S_in = S_in;
     prm.S_out = S_out;
     prm.y_dbg = y_debug;
     prm.cnt = reinterpret_cast<unsigned*>(xl.use);
-    prm.rn = xl.use + flag_cnt_words(B, N);
+    prm.rn = xl.use + flag_cnt_words(total);
     prm.part = xl.part;
     prm.xch_clear = reinterpret_cast<uint4*>(xl.clear);
     prm.n_clear4 = static_cast<int64_t>(xl.clear_words / 4);
     prm.status = ws.status;
+    prm.items = items;
     prm.B = B;
     prm.H = H;
     prm.N = N;
-    prm.Nc = static_cast<int>(Nc);
+    prm.Nc = static_cast<int>((N + CH - 1) / CH);
+    prm.total = total;
     prm.eps = eps;
     prm.inv_width = 1.0f / static_cast<float>(H * D);
     cudaLaunchConfig_t cfg = {};
@@ -888,13 +956,34 @@ int launch_prefill_tc(const void* q, const void* k, const void* v, const void* g
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, k_prefill_tc, mq, mk, mv, mg, mo, prm) != cudaSuccess) {
+    const cudaError_t e =
+        items ? cudaLaunchKernelEx(&cfg, k_prefill_tc<true>, mq, mk, mv, mg, mo, prm)
+              : cudaLaunchKernelEx(&cfg, k_prefill_tc<false>, mq, mk, mv, mg, mo, prm);
+    if (e != cudaSuccess) {
         cudaGetLastError();
         return LA_ERR_CUDA;
     }
-    xch_commit(xl, prefill_tc_flag_words(B, H, N));
+    xch_commit(xl, flag_words_for(total));
     note_launches(1);
     return LA_OK;
+}
+
+}  // namespace
+
+int launch_prefill_tc(const void* q, const void* k, const void* v, const void* g, void* out,
+                      const float* S_in, float* S_out, float* y_debug, int B, int H, int64_t N,
+                      float eps, const Workspace& ws, const XchLease& xl, cudaStream_t st) {
+    const int total = static_cast<int>(static_cast<int64_t>(B) * ((N + CH - 1) / CH));
+    return launch_items(q, k, v, g, out, S_in, S_out, y_debug, B, H, N, total, nullptr, eps, ws,
+                        xl, st);
+}
+
+int launch_prefill_tc_varlen(const void* q, const void* k, const void* v, const void* g,
+                             void* out, const float* S_in, float* S_out, float* y_debug, int H,
+                             int64_t T, int total, const int4* items, float eps,
+                             const Workspace& ws, const XchLease& xl, cudaStream_t st) {
+    return launch_items(q, k, v, g, out, S_in, S_out, y_debug, 1, H, T, total, items, eps, ws, xl,
+                        st);
 }
 
 }  // namespace la

@@ -10,7 +10,12 @@ Tolerances (bf16 I/O with fp32 accumulation / fp32 I/O):
   head's row can cancel (q^ . k^ sums 128 terms of both signs), so a bound relative
   to that row's own maximum is not met by any bf16-operand product; the elementwise
   bound is the standard forward-error bound of a dot product and holds in every row.
-* state: max|dS| <= 5e-3 * max|S_ref|                     (fp32 I/O: 1e-5)
+* state, elementwise: |dS| <= 1e-2 * S_abs + 1e-6 * max(S_abs)  (fp32 I/O: 1e-5), with
+  S_abs = |S0| + sum_s |k^_s|^T |v^_s|: one bf16 rounding (unit roundoff 2^-8) of each
+  MMA operand bounds a single product's relative error by 2^-7, so a sequence of a few
+  tokens can reach ~0.8% of its largest element;
+  and for sequences of >= 128 tokens, where the roundings average out, also
+  max|dS| <= 5e-3 * max|S_ref|                              (fp32 I/O: 1e-5)
 """
 import numpy as np
 
@@ -53,6 +58,28 @@ def y_abs_bound(orc, q, k, v, S0=None):
     qa, ka, va = (np.abs(orc.silu(x)) for x in (q, k, v))
     y, _ = orc.core(qa, ka, va, S0=None if S0 is None else np.abs(S0))
     return y
+
+
+def state_abs_bound(orc, k, v, S0=None):
+    """S_abs = |S0| + sum over tokens of |SiLU(k)|^T |SiLU(v)| per (b, h)."""
+    ka, va = (np.abs(orc.silu(x)) for x in (k, v))
+    _, S = orc.core(ka, ka, va, S0=None if S0 is None else np.abs(S0), want_y=False)
+    return S
+
+
+def state_ok(orc, got, ref, k, v, S0, dt):
+    """The state checks above; returns (ok, message)."""
+    tol = TOL[dt]
+    n = np.asarray(k).shape[1]
+    sabs = state_abs_bound(orc, k, v, S0)
+    ok, worst = elem_bound_ok(got, ref, sabs, tol["y_elem"])
+    if not ok:
+        return False, f"state exceeds the elementwise bound by x{worst:.2f}"
+    if n >= 128:
+        e = rel_max_err(got, ref)
+        if e > tol["state"]:
+            return False, f"state rel err {e:.3e}"
+    return True, ""
 
 
 def elem_bound_ok(got, ref, yabs, rel):

@@ -37,6 +37,7 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for want in ["la_prefill", "la_decode_step", "la_prefill_ex", "la_decode_step_ex",
+                 "la_prefill_varlen", "la_prefill_varlen_ex",
                  "la_status_string", "la_get_device_status", "la_version", "la_launch_count",
                  "la_prefill_path"]:
         assert want in names
@@ -121,6 +122,21 @@ def test_prefill_path_rejects_on_host(lib):
     assert lib.la_prefill_path(1, 1, 1, 128, 9, 0) == -la.LA_ERR_INVALID_ARG
     assert lib.la_prefill_path(1, 1, 1, 128, la.LA_F32, 0) == 1   # fp32: CUDA-core kernel
     assert lib.la_prefill_path(1, 1, 1, 128, la.LA_BF16, la.LA_FLAG_SIMT) == 1
+
+
+@pytest.mark.parametrize("cu,S,d,want", [
+    ([0, 5, 3], 2, 128, la.LA_ERR_INVALID_ARG),     # decreasing offsets
+    ([1, 5], 1, 128, la.LA_ERR_INVALID_ARG),        # does not start at 0
+    ([0, 5], 0, 128, la.LA_ERR_INVALID_ARG),        # no sequence
+    ([0, 5], 1, 64, la.LA_ERR_UNSUPPORTED),         # head size
+])
+def test_varlen_rejects_on_host(lib, cu, S, d, want):
+    arr = (ctypes.c_int64 * len(cu))(*cu)
+    rc = lib.la_prefill_varlen_ex(P[0], P[1], P[2], P[3], P[4], P[5], None, None, arr, S, 2, d,
+                                  la.LA_BF16, 1e-6, 0, None)
+    assert rc == want
+    assert lib.la_prefill_varlen_ex(P[0], P[1], P[2], P[3], P[4], P[5], None, None, None, 1, 2,
+                                    128, la.LA_BF16, 1e-6, 0, None) == la.LA_ERR_INVALID_ARG
 
 
 def test_decode_entry_rejects_on_host(lib):
