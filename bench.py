@@ -12,6 +12,8 @@ is needed between steps.  Printed as one JSON line:
 * ``roofline``: the dominant kernel's algorithmic bytes / its measured duration
   against the measured HBM copy bandwidth
 * ``decode``: the batched decode workload (B=256, H=64, d=128, fp32 state), GB/s
+* ``varlen``: a packed batch of 64K tokens in sequences of seeded lengths (1..8192)
+  through ``la_prefill_varlen``, tokens/s and GB/s
 * ``e2e``: the same prefill with pinned host inputs, the H2D copies and the D2H
   copy of the output inside the timed region
 * ``cpu_baseline``: the fp64 oracle on a bounded sample, on this host's cores
@@ -45,6 +47,7 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="prefill_8k")
     ap.add_argument("--simt", action="store_true", help="time the CUDA-core prefill kernel")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-varlen", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -203,9 +206,10 @@ class ClockSampler:
         return d
 
 
-def kernel_traffic(kernel: str, source_files):
+def kernel_traffic(kernel: str, source_files, workload: str):
     """dram bytes per launch from a committed ncu summary, if it was taken on the
-    current kernel source (the summary records the sources' sha256)."""
+    current kernel source (the summary records the sources' sha256) and on this
+    workload."""
     h = hashlib.sha256()
     for p in source_files:
         with open(p, "rb") as f:
@@ -220,7 +224,7 @@ def kernel_traffic(kernel: str, source_files):
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip()
-    if vals.get("source_sha256_16") != digest:
+    if vals.get("source_sha256_16") != digest or vals.get("workload") != workload:
         return None, digest
     try:
         return float(vals["dram_bytes_per_launch"]), digest
@@ -356,7 +360,7 @@ def run_ours(a):
     src = [os.path.join(ROOT, "linear_attention_hybrid_fwd_b300", "csrc", f)
            for f in ("la_simt.cu",) if a.simt] or [
         os.path.join(ROOT, "linear_attention_hybrid_fwd_b300", "csrc", "la_prefill_tc.cu")]
-    traffic, digest = kernel_traffic(kern, src)
+    traffic, digest = kernel_traffic(kern, src, w.name)
     achieved = io_bytes / (ms_local / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -379,6 +383,9 @@ def run_ours(a):
     if not a.no_decode:
         line["decode"] = bench_decode(a, torch, la, WORKLOADS["decode_b256"], dev, stream,
                                       peaks, make_decode_inputs, rank)
+    if not a.no_varlen:
+        line["varlen"] = bench_varlen(a, torch, la, WORKLOADS["prefill_varlen_64k"], dev,
+                                      stream, peaks, make_prefill_inputs, rank)
     if not a.no_e2e:
         line["e2e"] = bench_e2e(a, torch, la, q, k, v, g, out, S, stream, world, dev)
     del q, k, v, g, out
@@ -420,6 +427,41 @@ def bench_decode(a, torch, la, w, dev, stream, peaks, make_decode_inputs, rank):
     return {"workload": w.name, "B": w.B, "H": w.H, "d": w.d, "ms_per_step": ms,
             "bytes_per_step": nbytes, "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
             "tokens_per_s": w.B / (ms / 1e3), "gpu_launches_per_step": launches / len(per)}
+
+
+def bench_varlen(a, torch, la, w, dev, stream, peaks, make_prefill_inputs, rank):
+    """Packed prefill: w.N tokens in sequences of seeded lengths in [1, 8192], one
+    la_prefill_varlen call per step (its host-built chunk table upload included)."""
+    from linear_attention_hybrid_fwd_b300.inputs import varlen_lengths
+    lens = varlen_lengths(w.N, 1, 8192, w.seed)
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    q, k, v, g = (t[0] for t in make_prefill_inputs(1, w.N, w.H, w.d, torch.bfloat16,
+                                                      w.scale, w.seed + 100 * rank, dev))
+    out = torch.empty_like(q)
+    S = torch.empty((len(lens), w.H, w.d, w.d), device=dev, dtype=torch.float32)
+
+    def step():
+        la.la_prefill_varlen(q, k, v, g, cu, out=out, kv_state_out=S)
+
+    for _ in range(max(a.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if la.la_get_device_status() != 0:
+        raise SystemExit("device status error after the packed-batch warm-up")
+    n0 = la.la_launch_count()
+    per = time_steps(torch, step, max(min(a.steps, 100), 10), stream)
+    launches = la.la_launch_count() - n0
+    ms = sum(per) / len(per)
+    nbytes = 5.0 * w.N * w.H * w.d * 2 + len(lens) * w.H * w.d * w.d * 4
+    gbs = nbytes / (ms / 1e3) / 1e9
+    del q, k, v, g, out, S
+    return {"workload": w.name, "T": w.N, "num_seqs": len(lens), "H": w.H, "d": w.d,
+            "lengths": "uniform in [1, 8192], numpy default_rng(%d)" % w.seed,
+            "ms_per_step": ms, "tokens_per_s": w.N / (ms / 1e3), "bytes_per_step": nbytes,
+            "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
+            "gpu_launches_per_step": launches / len(per)}
 
 
 def bench_e2e(a, torch, la, q, k, v, g, out, S, stream, world, dev):

@@ -38,7 +38,22 @@ WORKLOADS = {
     "decode_b256": Workload("decode_b256", 256, 64, 1024, 128, "bf16", 0.5, 4, decode_steps=64),
     # 1M-token prefill
     "prefill_1m": Workload("prefill_1m", 1, 64, 1048576, 128, "bf16", 0.5, 5),
+    # packed batch: 64K tokens in sequences of seeded lengths (varlen_lengths)
+    "prefill_varlen_64k": Workload("prefill_varlen_64k", 1, 64, 65536, 128, "bf16", 0.5, 6),
 }
+
+
+def varlen_lengths(total: int, lo: int, hi: int, seed: int):
+    """Sequence lengths drawn uniformly from [lo, hi] (numpy default_rng(seed)) until
+    they sum to ``total``; the last one is cut to fit.  Returns a list of ints."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    lens, left = [], total
+    while left > 0:
+        n = min(int(rng.integers(lo, hi + 1)), left)
+        lens.append(n)
+        left -= n
+    return lens
 
 
 def torch_dtype(name: str):

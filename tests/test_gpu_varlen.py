@@ -96,3 +96,43 @@ def test_varlen_all_empty(env):
     _, S = la.la_prefill_varlen(q, q, q, q, [0, 0, 0, 0], kv_state_in=S_in)
     torch.cuda.synchronize()
     assert torch.equal(S, S_in)
+
+
+def test_varlen_bench_workload(env):
+    """The packed batch bench.py times (64K tokens, H64, 15 sequences of seeded lengths
+    in [1, 8192], one la_prefill_varlen launch): every sequence equals its own
+    la_prefill bitwise; every final state matches the fp64 state pass; the output is
+    checked against the oracle on the first 256 tokens of every sequence and on a
+    256-token window at the end of two sequences (from the fp64 state before it)."""
+    torch, la, orc = env
+    from oracle.state_pass import state_pass
+    from linear_attention_hybrid_fwd_b300.inputs import WORKLOADS, varlen_lengths
+    w = WORKLOADS["prefill_varlen_64k"]
+    lens = varlen_lengths(w.N, 1, 8192, w.seed)
+    cu = [0] + [int(x) for x in np.cumsum(lens)]
+    from linear_attention_hybrid_fwd_b300.inputs import make_prefill_inputs
+    q, k, v, g = (t[0] for t in make_prefill_inputs(1, w.N, w.H, w.d, torch.bfloat16,
+                                                      w.scale, w.seed, "cuda"))
+    out, S = la.la_prefill_varlen(q, k, v, g, cu)
+    torch.cuda.synchronize()
+    assert la.la_get_device_status() == 0
+    W = 256
+    for b, n in enumerate(lens):
+        r0, r1 = cu[b], cu[b + 1]
+        sl = [t[r0:r1].unsqueeze(0).contiguous() for t in (q, k, v, g)]
+        o_b, S_b = la.la_prefill(*sl)
+        torch.cuda.synchronize()
+        assert torch.equal(out[r0:r1], o_b[0]), f"sequence {b}: differs from its own prefill"
+        assert torch.equal(S[b], S_b[0]), f"sequence {b}: state differs from its own prefill"
+        S_ref = state_pass(sl[1].cpu(), sl[2].cpu())
+        e_S = rel_max_err(host64(S[b:b + 1]), S_ref)
+        assert e_S <= TOL["bf16"]["state"], f"sequence {b}: state rel err {e_S:.3e}"
+        ref_out, _, _ = orc.prefill(*(host64(t[:, :W]) for t in sl))
+        e = rel_max_err(host64(out[r0:r0 + W]), ref_out[0])
+        assert e <= TOL["bf16"]["out"], f"sequence {b}: head window rel err {e:.3e}"
+        if b in (0, len(lens) - 1):
+            t0 = n - W
+            S0 = state_pass(sl[1][:, :t0].cpu(), sl[2][:, :t0].cpu())
+            ref_out, _, _ = orc.prefill(*(host64(t[:, t0:]) for t in sl), S0=S0)
+            e = rel_max_err(host64(out[r0 + t0:r1]), ref_out[0])
+            assert e <= TOL["bf16"]["out"], f"sequence {b}: tail window rel err {e:.3e}"
