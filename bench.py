@@ -12,6 +12,10 @@ is needed between steps.  Printed as one JSON line:
 * ``roofline``: the dominant kernel's algorithmic bytes / its measured duration
   against the measured HBM copy bandwidth
 * ``decode``: the batched decode workload (B=256, H=64, d=128, fp32 state), GB/s
+* ``projection``: the input projection x [8192, 6144] -> q, k, v, g [8192, 64, 128]
+  (la_qkvg_projection with SiLU), TFLOP/s against the measured bf16 peak, with
+  cuBLAS (torch.matmul, no epilogue) on the same shapes beside it, and the layer from x
+  (projection + la_prefill on the activated outputs)
 * ``varlen``: a packed batch of 64K tokens in sequences of seeded lengths (1..8192)
   through ``la_prefill_varlen``, tokens/s and GB/s
 * ``e2e``: the same prefill with pinned host inputs, the H2D copies and the D2H
@@ -48,6 +52,7 @@ def parse_args(argv=None):
     ap.add_argument("--simt", action="store_true", help="time the CUDA-core prefill kernel")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-varlen", action="store_true")
+    ap.add_argument("--no-projection", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -383,6 +388,9 @@ def run_ours(a):
     if not a.no_decode:
         line["decode"] = bench_decode(a, torch, la, WORKLOADS["decode_b256"], dev, stream,
                                       peaks, make_decode_inputs, rank)
+    if not a.no_projection:
+        line["projection"] = bench_projection(a, torch, la, WORKLOADS["proj_8k"], dev, stream,
+                                              peaks, rank)
     if not a.no_varlen:
         line["varlen"] = bench_varlen(a, torch, la, WORKLOADS["prefill_varlen_64k"], dev,
                                       stream, peaks, make_prefill_inputs, rank)
@@ -427,6 +435,64 @@ def bench_decode(a, torch, la, w, dev, stream, peaks, make_decode_inputs, rank):
     return {"workload": w.name, "B": w.B, "H": w.H, "d": w.d, "ms_per_step": ms,
             "bytes_per_step": nbytes, "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
             "tokens_per_s": w.B / (ms / 1e3), "gpu_launches_per_step": launches / len(per)}
+
+
+def bench_projection(a, torch, la, w, dev, stream, peaks, rank):
+    """x [T, hidden] -> q, k, v, g [T, H, d] with SiLU on q, k, v (one launch), then the
+    same x through the whole layer (projection + prefill of the activated outputs)."""
+    from linear_attention_hybrid_fwd_b300.inputs import make_projection_inputs
+    x, wt = make_projection_inputs(w.N, w.hidden, w.H, w.d, w.seed + 100 * rank, dev)
+    outs = tuple(torch.empty((w.N, w.H, w.d), device=dev, dtype=torch.bfloat16)
+                 for _ in range(4))
+    steps = max(min(a.steps, 50), 10)
+
+    def proj():
+        la.la_qkvg_projection(x, wt, w.H, activate=True, out=outs)
+
+    for _ in range(max(a.warmup, 3)):
+        proj()
+    torch.cuda.synchronize()
+    if la.la_get_device_status() != 0:
+        raise SystemExit("device status error after the projection warm-up")
+    n0 = la.la_launch_count()
+    ms = sum(time_steps(torch, proj, steps, stream)) / steps
+    launches = (la.la_launch_count() - n0) / steps
+    flops = 2.0 * w.N * w.hidden * 4 * w.H * w.d
+    tflops = flops / (ms / 1e3) / 1e12
+    # cuBLAS on the same product, for context (no SiLU, one [T, 4Hd] output)
+    y = torch.empty((w.N, 4 * w.H * w.d), device=dev, dtype=torch.bfloat16)
+
+    def cublas():
+        torch.matmul(x, wt.t(), out=y)
+
+    for _ in range(3):
+        cublas()
+    ms_cublas = sum(time_steps(torch, cublas, steps, stream)) / steps
+    del y
+    # the layer from x: projection, then the prefill on the activated outputs
+    o = torch.empty((1, w.N, w.H, w.d), device=dev, dtype=torch.bfloat16)
+    S = torch.empty((1, w.H, w.d, w.d), device=dev, dtype=torch.float32)
+    q4 = tuple(t.unsqueeze(0) for t in outs)
+
+    def layer():
+        proj()
+        la.la_prefill(*q4, out=o, kv_state_out=S, activated=True)
+
+    for _ in range(3):
+        layer()
+    torch.cuda.synchronize()
+    ms_layer = sum(time_steps(torch, layer, steps, stream)) / steps
+    del x, wt, outs, o, S
+    return {"workload": w.name, "T": w.N, "hidden": w.hidden, "H": w.H, "d": w.d,
+            "ms_per_step": ms, "tflops": tflops,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"],
+                         "kernel": "la_qkvg_projection",
+                         "flops_per_launch": flops},
+            "cublas_ms": ms_cublas, "cublas_tflops": flops / (ms_cublas / 1e3) / 1e12,
+            "layer_from_x_ms": ms_layer,
+            "layer_from_x_tokens_per_s": w.N / (ms_layer / 1e3),
+            "gpu_launches_per_step": launches}
 
 
 def bench_varlen(a, torch, la, w, dev, stream, peaks, make_prefill_inputs, rank):

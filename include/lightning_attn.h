@@ -60,6 +60,9 @@ typedef enum {
 /* Flags for the _ex entry points. */
 #define LA_FLAG_SIMT 1u /* prefill: run the CUDA-core kernel instead of the
                            tensor-core kernel (the only kernel for LA_F32) */
+#define LA_FLAG_ACTIVATED 2u /* prefill: q, k, v are already SiLU-activated (as
+                                la_qkvg_projection writes them with LA_PROJ_SILU);
+                                the kernels skip step 2.  g is raw either way. */
 
 /*
  * Prefill of B sequences of N tokens ("Hybrid Modeling", mechanism steps 2-4).
@@ -175,6 +178,30 @@ const char* la_status_string(int status);
 /* Synchronises cuda_stream, returns and clears the device status word of the current
    device (LA_OK or LA_ERR_TIMEOUT), or LA_ERR_CUDA if synchronisation failed. */
 int la_get_device_status(void* cuda_stream);
+
+/*
+ * Input projection of the layer on tensor cores: the step before the path
+ * ("Hybrid Modeling", MiniMax-01 deep dive: step 1 "Input X", step 2 "Q, K, V =
+ * SiLU(X)", the projections being the part the printed step leaves out; hidden size
+ * 6144 in MiniMax-Text-01, the model card's "Model Architecture" list):
+ *     [q | k | v | g] = x W^T,  then SiLU on q, k, v when flags has LA_PROJ_SILU
+ *   x        in  [T][hidden] bf16, row-major
+ *   w        in  [4*H*d][hidden] bf16, row-major: rows [0, Hd) make q, [Hd, 2Hd) k,
+ *                [2Hd, 3Hd) v, [3Hd, 4Hd) g (a fused bias-free linear layer's weight)
+ *   q,k,v,g  out [T][H][d] bf16 each: the layout la_prefill reads.  g is never
+ *                activated (the layer applies sigmoid to it after the norm).
+ *   flags    0 or LA_PROJ_SILU; with it the outputs are la_prefill_ex's
+ *            LA_FLAG_ACTIVATED inputs, without it la_prefill's raw inputs
+ * fp32 accumulation; each output element is rounded once to bf16 (RNE).  d must be 128
+ * and H even (H*d a multiple of 256), hidden a multiple of 8 (LA_ERR_UNSUPPORTED
+ * otherwise).  All pointers are device pointers, 16-byte aligned; the caller owns them;
+ * no output may overlap x, w or another output.  T = 0 does nothing.  Argument errors
+ * are returned before any launch; a bounded device wait that gives up records
+ * LA_ERR_TIMEOUT in the device status word.
+ */
+#define LA_PROJ_SILU 1u
+int la_qkvg_projection(const void* x, const void* w, void* q, void* k, void* v, void* g,
+                       int64_t T, int hidden, int H, int d, unsigned flags, void* cuda_stream);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int la_version(void);

@@ -21,15 +21,18 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["la_prefill", "la_prefill_varlen", "la_decode_step", "la_decode_step_noalloc", "la_status_string", "la_get_device_status",
-           "la_version", "la_launch_count", "la_prefill_path", "LaError", "library_path",
-           "load_library", "LA_BF16", "LA_F32", "LA_FLAG_SIMT"]
+__all__ = ["la_prefill", "la_prefill_varlen", "la_decode_step", "la_decode_step_noalloc",
+           "la_qkvg_projection", "la_status_string", "la_get_device_status", "la_version",
+           "la_launch_count", "la_prefill_path", "LaError", "library_path", "load_library",
+           "LA_BF16", "LA_F32", "LA_FLAG_SIMT", "LA_FLAG_ACTIVATED", "LA_PROJ_SILU"]
 
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_MISALIGNED = 0, 1, 2, 3
 LA_ERR_CUDA, LA_ERR_NOMEM, LA_ERR_TIMEOUT, LA_ERR_SCRATCH_LIMIT = 4, 5, 6, 7
 LA_NOALLOC_MAX_HEADS = 16384
 LA_BF16, LA_F32 = 0, 1
 LA_FLAG_SIMT = 1
+LA_FLAG_ACTIVATED = 2
+LA_PROJ_SILU = 1
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "liblightning_attn.so")
@@ -82,6 +85,8 @@ def load_library():
     lib.la_version.restype = i32
     lib.la_prefill_path.argtypes = [i32, i32, i64, i32, i32, u32]
     lib.la_prefill_path.restype = i32
+    lib.la_qkvg_projection.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, u32, vp]
+    lib.la_qkvg_projection.restype = i32
     lib.la_launch_count.argtypes = []
     lib.la_launch_count.restype = ctypes.c_int64
     _lib = lib
@@ -146,14 +151,20 @@ def _check(ts, names):
             raise ValueError(f"{n} is on {t.device}, expected {dev}")
 
 
+def _prefill_flags(simt, activated):
+    return (LA_FLAG_SIMT if simt else 0) | (LA_FLAG_ACTIVATED if activated else 0)
+
+
 def la_prefill(q, k, v, g, out=None, kv_state_out=None, kv_state_in=None, y_debug=None,
-               eps: float = 1e-6, simt: bool = False, want_state: bool = True, stream=None):
+               eps: float = 1e-6, simt: bool = False, want_state: bool = True, stream=None,
+               activated: bool = False):
     """Prefill. ``q, k, v, g``: ``[B, N, H, d]`` (bf16 or fp32, contiguous, CUDA).
 
     Returns ``(out, kv_state_out)``; ``kv_state_out`` is ``[B, H, d, d]`` fp32 (``None``
     when ``want_state`` is False and none was passed).  ``kv_state_in`` continues a
     sequence from a previous state; ``y_debug`` (fp32 ``[B, N, H, d]``) receives the
-    pre-norm output.  ``simt`` selects the CUDA-core kernel.
+    pre-norm output.  ``simt`` selects the CUDA-core kernel.  ``activated``: q, k, v
+    are already SiLU-activated (``la_qkvg_projection(..., activate=True)``).
     """
     import torch
     B, N, H, d = q.shape
@@ -173,7 +184,7 @@ def la_prefill(q, k, v, g, out=None, kv_state_out=None, kv_state_in=None, y_debu
         raise ValueError("y_debug must be float32 [B, N, H, d]")
     rc = load_library().la_prefill_ex(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out), _ptr(kv_state_out), _ptr(kv_state_in),
-        _ptr(y_debug), B, H, N, d, _dtype_code(q), float(eps), LA_FLAG_SIMT if simt else 0,
+        _ptr(y_debug), B, H, N, d, _dtype_code(q), float(eps), _prefill_flags(simt, activated),
         _stream_handle(stream))
     if rc != LA_OK:
         raise LaError(rc, "la_prefill")
@@ -182,7 +193,7 @@ def la_prefill(q, k, v, g, out=None, kv_state_out=None, kv_state_in=None, y_debu
 
 def la_prefill_varlen(q, k, v, g, cu_seqlens, out=None, kv_state_out=None, kv_state_in=None,
                       y_debug=None, eps: float = 1e-6, simt: bool = False, want_state: bool = True,
-                      stream=None):
+                      stream=None, activated: bool = False):
     """Packed prefill: ``q, k, v, g`` are ``[T, H, d]`` (bf16 or fp32, contiguous, CUDA),
     sequence ``b`` is rows ``cu_seqlens[b]:cu_seqlens[b+1]`` (``cu_seqlens``: host ints,
     ``num_seqs + 1`` of them, starting at 0).  Returns ``(out, kv_state_out)`` with
@@ -213,11 +224,41 @@ def la_prefill_varlen(q, k, v, g, cu_seqlens, out=None, kv_state_out=None, kv_st
     cu_arr = (ctypes.c_int64 * (S + 1))(*cu)
     rc = load_library().la_prefill_varlen_ex(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out), _ptr(kv_state_out), _ptr(kv_state_in),
-        _ptr(y_debug), cu_arr, S, H, d, _dtype_code(q), float(eps), LA_FLAG_SIMT if simt else 0,
+        _ptr(y_debug), cu_arr, S, H, d, _dtype_code(q), float(eps), _prefill_flags(simt, activated),
         _stream_handle(stream))
     if rc != LA_OK:
         raise LaError(rc, "la_prefill_varlen")
     return out, kv_state_out
+
+
+def la_qkvg_projection(x, w, H: int, d: int = 128, activate: bool = True, out=None,
+                       stream=None):
+    """Input projection on tensor cores: ``x`` ``[T, hidden]`` bf16, ``w`` ``[4*H*d,
+    hidden]`` bf16 (rows: q, k, v, g features).  Returns ``(q, k, v, g)``, each bf16
+    ``[T, H, d]``; q, k, v are SiLU-activated when ``activate`` (feed them to
+    ``la_prefill(..., activated=True)``), otherwise raw.  ``out``: optional tuple of four
+    preallocated outputs."""
+    import torch
+    if x.dim() != 2 or w.dim() != 2:
+        raise ValueError("x must be [T, hidden] and w [4*H*d, hidden]")
+    T, hidden = x.shape
+    if tuple(w.shape) != (4 * H * d, hidden):
+        raise ValueError(f"w must be [{4 * H * d}, {hidden}], got {tuple(w.shape)}")
+    if out is None:
+        out = tuple(torch.empty((T, H, d), device=x.device, dtype=x.dtype) for _ in range(4))
+    _check([x, w, *out], ["x", "w", "q", "k", "v", "g"])
+    for t in (x, w, *out):
+        if t.dtype != torch.bfloat16:
+            raise ValueError("la_qkvg_projection takes and returns bf16 tensors")
+    for t in out:
+        if tuple(t.shape) != (T, H, d):
+            raise ValueError(f"outputs must be [{T}, {H}, {d}]")
+    rc = load_library().la_qkvg_projection(
+        _ptr(x), _ptr(w), *(_ptr(t) for t in out), T, hidden, H, d,
+        LA_PROJ_SILU if activate else 0, _stream_handle(stream))
+    if rc != LA_OK:
+        raise LaError(rc, "la_qkvg_projection")
+    return out
 
 
 def la_decode_step(kv_state, q, k, v, g, out=None, y_debug=None, eps: float = 1e-6,

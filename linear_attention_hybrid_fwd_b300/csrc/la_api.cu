@@ -222,7 +222,7 @@ int la_prefill_ex(const void* q, const void* k, const void* v, const void* g, vo
     if (B <= 0 || H <= 0 || N < 0 || d <= 0) return LA_ERR_INVALID_ARG;
     if (dtype != LA_BF16 && dtype != LA_F32) return LA_ERR_INVALID_ARG;
     if (!(eps >= 0.0f) || !isfinite(eps)) return LA_ERR_INVALID_ARG;
-    if (flags & ~LA_FLAG_SIMT) return LA_ERR_INVALID_ARG;
+    if (flags & ~(LA_FLAG_SIMT | LA_FLAG_ACTIVATED)) return LA_ERR_INVALID_ARG;
     if (d != kHeadDim) return LA_ERR_UNSUPPORTED;
     if (B > 65535 || H > 4096) return LA_ERR_UNSUPPORTED;
     // element counts: B*N*H*d must stay well inside int64 (the kernels index in int64)
@@ -269,7 +269,7 @@ int la_prefill_ex(const void* q, const void* k, const void* v, const void* g, vo
         rc = xch_acquire(prefill_tc_flag_words(items), prefill_tc_part_floats(items, H), st, &xl);
         if (rc != LA_OK) return rc;
         return launch_prefill_tc(q, k, v, g, out, kv_state_in, kv_state_out, y_debug, B, H, N,
-                                 eps, ws, xl, st);
+                                 eps, (flags & LA_FLAG_ACTIVATED) != 0, ws, xl, st);
     }
     // CUDA-core kernel: y in fp32 (into y_debug when given), then the norm/gate pass.
     float* y = y_debug;
@@ -279,7 +279,8 @@ int la_prefill_ex(const void* q, const void* k, const void* v, const void* g, vo
         if (rc != LA_OK) return rc;
         y = static_cast<float*>(ws.base);
     }
-    int rc = launch_prefill_simt(q, k, v, kv_state_in, y, kv_state_out, B, H, N, bf16, st);
+    int rc = launch_prefill_simt(q, k, v, kv_state_in, y, kv_state_out, B, H, N, bf16,
+                                 (flags & LA_FLAG_ACTIVATED) != 0, st);
     if (rc != LA_OK) return rc;
     return launch_norm_gate_rows(y, g, out, (int64_t)B * N, H * d, eps, bf16, st);
 }
@@ -287,7 +288,7 @@ int la_prefill_ex(const void* q, const void* k, const void* v, const void* g, vo
 int la_prefill_path(int B, int H, int64_t N, int d, int dtype, unsigned flags) {
     if (B <= 0 || H <= 0 || N < 0 || d <= 0) return -LA_ERR_INVALID_ARG;
     if (dtype != LA_BF16 && dtype != LA_F32) return -LA_ERR_INVALID_ARG;
-    if (flags & ~LA_FLAG_SIMT) return -LA_ERR_INVALID_ARG;
+    if (flags & ~(LA_FLAG_SIMT | LA_FLAG_ACTIVATED)) return -LA_ERR_INVALID_ARG;
     if (d != kHeadDim) return -LA_ERR_UNSUPPORTED;
     const bool tc = dtype == LA_BF16 && !(flags & LA_FLAG_SIMT) && N > 0 &&
                     prefill_tc_supported(B, H, N) == LA_OK;
@@ -308,7 +309,7 @@ int la_prefill_varlen_ex(const void* q, const void* k, const void* v, const void
     if (num_seqs <= 0 || H <= 0 || d <= 0 || !cu_seqlens) return LA_ERR_INVALID_ARG;
     if (dtype != LA_BF16 && dtype != LA_F32) return LA_ERR_INVALID_ARG;
     if (!(eps >= 0.0f) || !isfinite(eps)) return LA_ERR_INVALID_ARG;
-    if (flags & ~LA_FLAG_SIMT) return LA_ERR_INVALID_ARG;
+    if (flags & ~(LA_FLAG_SIMT | LA_FLAG_ACTIVATED)) return LA_ERR_INVALID_ARG;
     if (d != kHeadDim) return LA_ERR_UNSUPPORTED;
     if (num_seqs > 65535 || H > 4096) return LA_ERR_UNSUPPORTED;
     if (cu_seqlens[0] != 0) return LA_ERR_INVALID_ARG;
@@ -375,7 +376,8 @@ int la_prefill_varlen_ex(const void* q, const void* k, const void* v, const void
         rc = items_upload(items, st, &dev_items);
         if (rc != LA_OK) return rc;
         return launch_prefill_tc_varlen(q, k, v, g, out, kv_state_in, kv_state_out, y_debug, H,
-                                        T, total, dev_items, eps, ws, xl, st);
+                                        T, total, dev_items, eps, (flags & LA_FLAG_ACTIVATED) != 0, ws,
+                                        xl, st);
     }
     // CUDA-core kernel (fp32 I/O, or on request): one prefill per sequence
     const size_t row = (size_t)H * d;  // elements per token

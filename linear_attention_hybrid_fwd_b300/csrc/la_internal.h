@@ -55,9 +55,10 @@ void note_launches(int n);
 
 // ---- CUDA-core kernels (la_simt.cu) ----------------------------------------------
 // Prefill: y (fp32 [B][N][H][d]) and the final state; then the norm/gate pass.
+// activated: q, k, v are already SiLU-activated (step 2 is skipped).
 int launch_prefill_simt(const void* q, const void* k, const void* v, const float* S_in,
                         float* y, float* S_out, int B, int H, int64_t N, bool bf16,
-                        cudaStream_t st);
+                        bool activated, cudaStream_t st);
 int launch_norm_gate_rows(const float* y, const void* g, void* out, int64_t rows, int width,
                           float eps, bool bf16, cudaStream_t st);
 // Decode: state update + y = q S (y fp32 [B][H][d], per-(b,h) sum of squares), and the
@@ -77,13 +78,15 @@ size_t prefill_tc_flag_words(int items);
 size_t prefill_tc_part_floats(int items, int H);
 int launch_prefill_tc(const void* q, const void* k, const void* v, const void* g, void* out,
                       const float* S_in, float* S_out, float* y_debug, int B, int H, int64_t N,
-                      float eps, const Workspace& ws, const XchLease& xl, cudaStream_t st);
+                      float eps, bool activated, const Workspace& ws, const XchLease& xl,
+                      cudaStream_t st);
 // A packed batch of T tokens: items (device, `total` of them) = {first row, valid rows,
 // sequence, first chunk of its sequence}, chunks of 128 tokens in order.
 int launch_prefill_tc_varlen(const void* q, const void* k, const void* v, const void* g,
                              void* out, const float* S_in, float* S_out, float* y_debug, int H,
                              int64_t T, int total, const int4* items, float eps,
-                             const Workspace& ws, const XchLease& xl, cudaStream_t st);
+                             bool activated, const Workspace& ws, const XchLease& xl,
+                             cudaStream_t st);
 // Chunk length of the tensor-core prefill (the items' granularity).
 constexpr int kTcChunk = 128;
 

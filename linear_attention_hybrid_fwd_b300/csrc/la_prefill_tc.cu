@@ -317,8 +317,9 @@ __device__ void reducer(Shared& sh, const Params& p, int j, int R) {
 // ------------------------------------------------------------------ the kernel
 // kVarlen: the items come from the packed batch's table (p.items) rather than from the
 // uniform B x ceil(N / 128) grid of chunks; the uniform instance carries none of the
-// packed batch's checks.
-template <bool kVarlen>
+// packed batch's checks.  kAct: q, k, v arrive already SiLU-activated, and the
+// activation warps only zero the rows past a packed sequence's end and forward tiles.
+template <bool kVarlen, bool kAct>
 __global__ void __launch_bounds__(kThreads, 1)
     k_prefill_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg,
@@ -510,7 +511,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool live = !kVarlen || t < p.items[it].y;
             uint8_t* blk = sm + own_off + s * TILE + part * HALF;
             uint4 x[4];
-            if (live) {
+            if (kAct && live) {
+                // already activated: nothing to do
+            } else if (live) {
 #pragma unroll
                 for (int g4 = 0; g4 < 2; ++g4) {
 #pragma unroll
@@ -532,7 +535,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   peer_xin + s * 8);
             if (!group_wait(sh, p.status, &sh.rawv[s], ph, leader, 1, 256, 0)) break;
             uint8_t* vt = sm + OFF_VB + s * HALF;
-            if (live) {
+            if (kAct && live) {
+            } else if (live) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     x[j] = *reinterpret_cast<const uint4*>(vt + swz(t, 4 * part + j));
@@ -844,16 +848,20 @@ bool encode_io_map(CUtensorMap* m, const void* base, int B, int H, int64_t N) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <typename F>
+bool set_smem_attr(F* f) {
+    return cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(SMEM_DYN)) == cudaSuccess;
+}
+
 int max_active_clusters() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
     std::lock_guard<std::mutex> lock(g_occ_mutex);
     if (g_max_clusters[dev] != 0) return g_max_clusters[dev];
     int n = -1;
-    if (cudaFuncSetAttribute(k_prefill_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(SMEM_DYN)) == cudaSuccess &&
-        cudaFuncSetAttribute(k_prefill_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(SMEM_DYN)) == cudaSuccess) {
+    if (set_smem_attr(k_prefill_tc<false, false>) && set_smem_attr(k_prefill_tc<true, false>) &&
+        set_smem_attr(k_prefill_tc<false, true>) && set_smem_attr(k_prefill_tc<true, true>)) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2, 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
@@ -866,10 +874,18 @@ int max_active_clusters() {
         cfg.attrs = at;
         cfg.numAttrs = 1;
         int m = 0;
-        int m1 = 0;
-        if (cudaOccupancyMaxActiveClusters(&m, k_prefill_tc<false>, &cfg) == cudaSuccess &&
-            cudaOccupancyMaxActiveClusters(&m1, k_prefill_tc<true>, &cfg) == cudaSuccess)
-            n = m < m1 ? m : m1;
+        // the fewest co-resident clusters over the four instances
+        n = 1 << 30;
+        for (const void* f : {reinterpret_cast<const void*>(k_prefill_tc<false, false>),
+                              reinterpret_cast<const void*>(k_prefill_tc<true, false>),
+                              reinterpret_cast<const void*>(k_prefill_tc<false, true>),
+                              reinterpret_cast<const void*>(k_prefill_tc<true, true>)}) {
+            if (cudaOccupancyMaxActiveClusters(&m, f, &cfg) != cudaSuccess) {
+                n = -1;
+                break;
+            }
+            n = m < n ? m : n;
+        }
     }
     cudaGetLastError();
     g_max_clusters[dev] = n > 0 ? n : -1;
@@ -916,7 +932,7 @@ namespace {
 // a packed batch viewed as one slab of N tokens (items: the per-item table on device).
 int launch_items(const void* q, const void* k, const void* v, const void* g, void* out,
                  const float* S_in, float* S_out, float* y_debug, int B, int H, int64_t N,
-                 int total, const int4* items, float eps, const Workspace& ws,
+                 int total, const int4* items, float eps, bool activated, const Workspace& ws,
                  const XchLease& xl, cudaStream_t st) {
     const int R = reducers_for(H);
     if (R <= 0) return LA_ERR_UNSUPPORTED;
@@ -957,8 +973,14 @@ int launch_items(const void* q, const void* k, const void* v, const void* g, voi
     cfg.attrs = at;
     cfg.numAttrs = 1;
     const cudaError_t e =
-        items ? cudaLaunchKernelEx(&cfg, k_prefill_tc<true>, mq, mk, mv, mg, mo, prm)
-              : cudaLaunchKernelEx(&cfg, k_prefill_tc<false>, mq, mk, mv, mg, mo, prm);
+        items ? (activated
+                     ? cudaLaunchKernelEx(&cfg, k_prefill_tc<true, true>, mq, mk, mv, mg, mo, prm)
+                     : cudaLaunchKernelEx(&cfg, k_prefill_tc<true, false>, mq, mk, mv, mg, mo,
+                                          prm))
+              : (activated
+                     ? cudaLaunchKernelEx(&cfg, k_prefill_tc<false, true>, mq, mk, mv, mg, mo, prm)
+                     : cudaLaunchKernelEx(&cfg, k_prefill_tc<false, false>, mq, mk, mv, mg, mo,
+                                          prm));
     if (e != cudaSuccess) {
         cudaGetLastError();
         return LA_ERR_CUDA;
@@ -972,18 +994,20 @@ int launch_items(const void* q, const void* k, const void* v, const void* g, voi
 
 int launch_prefill_tc(const void* q, const void* k, const void* v, const void* g, void* out,
                       const float* S_in, float* S_out, float* y_debug, int B, int H, int64_t N,
-                      float eps, const Workspace& ws, const XchLease& xl, cudaStream_t st) {
+                      float eps, bool activated, const Workspace& ws, const XchLease& xl,
+                      cudaStream_t st) {
     const int total = static_cast<int>(static_cast<int64_t>(B) * ((N + CH - 1) / CH));
-    return launch_items(q, k, v, g, out, S_in, S_out, y_debug, B, H, N, total, nullptr, eps, ws,
-                        xl, st);
+    return launch_items(q, k, v, g, out, S_in, S_out, y_debug, B, H, N, total, nullptr, eps,
+                        activated, ws, xl, st);
 }
 
 int launch_prefill_tc_varlen(const void* q, const void* k, const void* v, const void* g,
                              void* out, const float* S_in, float* S_out, float* y_debug, int H,
                              int64_t T, int total, const int4* items, float eps,
-                             const Workspace& ws, const XchLease& xl, cudaStream_t st) {
-    return launch_items(q, k, v, g, out, S_in, S_out, y_debug, 1, H, T, total, items, eps, ws, xl,
-                        st);
+                             bool activated, const Workspace& ws, const XchLease& xl,
+                             cudaStream_t st) {
+    return launch_items(q, k, v, g, out, S_in, S_out, y_debug, 1, H, T, total, items, eps,
+                        activated, ws, xl, st);
 }
 
 }  // namespace la

@@ -77,7 +77,9 @@ __global__ void __launch_bounds__(256) k_prefill_simt(const T* __restrict__ q,
                                                       const float* __restrict__ S_in,
                                                       float* __restrict__ y,
                                                       float* __restrict__ S_out, int H,
-                                                      int64_t N) {
+                                                      int64_t N, int activated) {
+    // step 2 (SiLU) unless the inputs arrive activated
+    auto act = [activated](float x) { return activated ? x : silu_f(x); };
     extern __shared__ float smem[];
     float* Qs = smem;              // [C][LDQ]  q^ rows of the chunk
     float* Ks = Qs + C * LDQ;      // [C][LDQ]  k^ rows
@@ -102,8 +104,8 @@ __global__ void __launch_bounds__(256) k_prefill_simt(const T* __restrict__ q,
             float qv = 0.f, kv = 0.f;
             if (t < nc) {
                 const int64_t off = ((b * N + c0 + t) * H + h) * D + i;
-                qv = silu_f(ldf(q, off));
-                kv = silu_f(ldf(k, off));
+                qv = act(ldf(q, off));
+                kv = act(ldf(k, off));
             }
             Qs[t * LDQ + i] = qv;
             Ks[t * LDQ + i] = kv;
@@ -111,7 +113,7 @@ __global__ void __launch_bounds__(256) k_prefill_simt(const T* __restrict__ q,
         for (int idx = tid; idx < C * DV; idx += 256) {
             const int t = idx / DV, j = idx % DV;
             float vv = 0.f;
-            if (t < nc) vv = silu_f(ldf(v, ((b * N + c0 + t) * H + h) * D + j0 + j));
+            if (t < nc) vv = act(ldf(v, ((b * N + c0 + t) * H + h) * D + j0 + j));
             Vs[idx] = vv;
         }
         __syncthreads();
@@ -336,7 +338,7 @@ __global__ void k_zero(float* p, int64_t n) {
 
 int launch_prefill_simt(const void* q, const void* k, const void* v, const float* S_in,
                         float* y, float* S_out, int B, int H, int64_t N, bool bf16,
-                        cudaStream_t st) {
+                        bool activated, cudaStream_t st) {
     dim3 grid((unsigned)((int64_t)B * H), D / DV);
     if (bf16) {
         auto kern = k_prefill_simt<__nv_bfloat16>;
@@ -344,14 +346,15 @@ int launch_prefill_simt(const void* q, const void* k, const void* v, const float
                                  (int)kSimtSmem) != cudaSuccess)
             return LA_ERR_CUDA;
         kern<<<grid, 256, kSimtSmem, st>>>((const __nv_bfloat16*)q, (const __nv_bfloat16*)k,
-                                           (const __nv_bfloat16*)v, S_in, y, S_out, H, N);
+                                           (const __nv_bfloat16*)v, S_in, y, S_out, H, N,
+                                           activated ? 1 : 0);
     } else {
         auto kern = k_prefill_simt<float>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kSimtSmem) != cudaSuccess)
             return LA_ERR_CUDA;
         kern<<<grid, 256, kSimtSmem, st>>>((const float*)q, (const float*)k, (const float*)v,
-                                           S_in, y, S_out, H, N);
+                                           S_in, y, S_out, H, N, activated ? 1 : 0);
     }
     note_launches(1);
     return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;

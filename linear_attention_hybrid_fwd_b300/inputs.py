@@ -11,7 +11,7 @@ from __future__ import annotations
 
 from dataclasses import dataclass
 
-TENSOR_IDS = {"q": 0, "k": 1, "v": 2, "g": 3}
+TENSOR_IDS = {"q": 0, "k": 1, "v": 2, "g": 3, "x": 4, "w": 5}
 
 
 @dataclass(frozen=True)
@@ -25,6 +25,7 @@ class Workload:
     scale: float      # inputs are N(0, 1) * scale before the cast
     seed: int
     decode_steps: int = 0
+    hidden: int = 0   # input projection: width of the token's hidden vector
 
 
 WORKLOADS = {
@@ -38,6 +39,8 @@ WORKLOADS = {
     "decode_b256": Workload("decode_b256", 256, 64, 1024, 128, "bf16", 0.5, 4, decode_steps=64),
     # 1M-token prefill
     "prefill_1m": Workload("prefill_1m", 1, 64, 1048576, 128, "bf16", 0.5, 5),
+    # input projection of the 8K prefill: x [8192, 6144] -> q, k, v, g [8192, 64, 128]
+    "proj_8k": Workload("proj_8k", 1, 64, 8192, 128, "bf16", 1.0, 7, hidden=6144),
     # packed batch: 64K tokens in sequences of seeded lengths (varlen_lengths)
     "prefill_varlen_64k": Workload("prefill_varlen_64k", 1, 64, 65536, 128, "bf16", 0.5, 6),
 }
@@ -85,6 +88,19 @@ def make_prefill_inputs(B, N, H, d, dtype, scale, seed, device):
     """q, k, v, g of shape ``[B, N, H, d]``."""
     return tuple(make_tensor((B, N, H, d), dtype, scale, seed, TENSOR_IDS[n], device)
                  for n in ("q", "k", "v", "g"))
+
+
+def make_projection_inputs(T, hidden, H, d, seed, device, wscale=None):
+    """x ``[T, hidden]`` N(0,1) and the stacked weight ``[4*H*d, hidden]``
+    N(0,1)*wscale (default 0.5/sqrt(hidden), so each projected feature is about
+    N(0, 0.25), the spread of the prefill workloads' inputs), both bf16."""
+    import torch
+    if wscale is None:
+        wscale = 0.5 / hidden ** 0.5
+    x = make_tensor((1, T, hidden), torch.bfloat16, 1.0, seed, TENSOR_IDS["x"], device)[0]
+    w = make_tensor((1, 4 * H * d, hidden), torch.bfloat16, wscale, seed, TENSOR_IDS["w"],
+                    device)[0]
+    return x, w
 
 
 def make_decode_inputs(B, H, d, dtype, scale, seed, step, device):

@@ -37,7 +37,7 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for want in ["la_prefill", "la_decode_step", "la_prefill_ex", "la_decode_step_ex",
-                 "la_prefill_varlen", "la_prefill_varlen_ex",
+                 "la_prefill_varlen", "la_prefill_varlen_ex", "la_qkvg_projection",
                  "la_status_string", "la_get_device_status", "la_version", "la_launch_count",
                  "la_prefill_path"]:
         assert want in names
@@ -83,6 +83,8 @@ def _prefill(lib, B=1, H=2, N=16, d=128, dtype=la.LA_BF16, eps=1e-6, flags=0, q=
     (dict(eps=-1.0), la.LA_ERR_INVALID_ARG),
     (dict(eps=float("nan")), la.LA_ERR_INVALID_ARG),
     (dict(flags=0x100), la.LA_ERR_INVALID_ARG),
+    (dict(flags=4), la.LA_ERR_INVALID_ARG),
+    (dict(flags=la.LA_FLAG_ACTIVATED, d=64), la.LA_ERR_UNSUPPORTED),  # flag itself accepted
     (dict(q=ctypes.c_void_p(0)), la.LA_ERR_INVALID_ARG),
     (dict(q=MIS), la.LA_ERR_MISALIGNED),
     (dict(out=P[0]), la.LA_ERR_INVALID_ARG),           # out aliases q
@@ -160,3 +162,32 @@ def test_package_does_not_import_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), f
                 assert "la_oracle" not in src, f
+
+
+def _proj(lib, T=16, hidden=64, H=2, d=128, flags=la.LA_PROJ_SILU, x=None, q=None):
+    return lib.la_qkvg_projection(x if x is not None else P[0], P[1],
+                                  q if q is not None else P[2], P[3], P[4], P[5], T, hidden,
+                                  H, d, flags, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(T=-1), la.LA_ERR_INVALID_ARG),
+    (dict(hidden=0), la.LA_ERR_INVALID_ARG),
+    (dict(H=0), la.LA_ERR_INVALID_ARG),
+    (dict(d=64), la.LA_ERR_UNSUPPORTED),
+    (dict(H=1), la.LA_ERR_UNSUPPORTED),                # H*d not a multiple of 256
+    (dict(hidden=12), la.LA_ERR_UNSUPPORTED),          # rows not 16-byte strided
+    (dict(flags=2), la.LA_ERR_INVALID_ARG),
+    (dict(x=ctypes.c_void_p(0)), la.LA_ERR_INVALID_ARG),
+    (dict(x=MIS), la.LA_ERR_MISALIGNED),
+    (dict(q=P[0]), la.LA_ERR_INVALID_ARG),             # q aliases x
+    (dict(q=P[3]), la.LA_ERR_INVALID_ARG),             # q aliases k
+])
+def test_projection_rejects_on_host(lib, kw, want):
+    assert _proj(lib, **kw) == want
+
+
+def test_projection_empty_batch_launches_nothing(lib):
+    n0 = lib.la_launch_count()
+    assert _proj(lib, T=0) == la.LA_OK
+    assert lib.la_launch_count() == n0
