@@ -454,9 +454,12 @@ def bench_projection(a, torch, la, w, dev, stream, peaks, rank):
     torch.cuda.synchronize()
     if la.la_get_device_status() != 0:
         raise SystemExit("device status error after the projection warm-up")
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
     n0 = la.la_launch_count()
     ms = sum(time_steps(torch, proj, steps, stream)) / steps
     launches = (la.la_launch_count() - n0) / steps
+    clk = clocks.stop()
     flops = 2.0 * w.N * w.hidden * 4 * w.H * w.d
     tflops = flops / (ms / 1e3) / 1e12
     # cuBLAS on the same product, for context (no SiLU, one [T, 4Hd] output)
@@ -492,7 +495,7 @@ def bench_projection(a, torch, la, w, dev, stream, peaks, rank):
             "cublas_ms": ms_cublas, "cublas_tflops": flops / (ms_cublas / 1e3) / 1e12,
             "layer_from_x_ms": ms_layer,
             "layer_from_x_tokens_per_s": w.N / (ms_layer / 1e3),
-            "gpu_launches_per_step": launches}
+            "gpu_launches_per_step": launches, "clocks": clk}
 
 
 def bench_varlen(a, torch, la, w, dev, stream, peaks, make_prefill_inputs, rank):
