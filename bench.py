@@ -16,6 +16,8 @@ is needed between steps.  Printed as one JSON line:
   (la_qkvg_projection with SiLU), TFLOP/s against the measured bf16 peak, with
   cuBLAS (torch.matmul, no epilogue) on the same shapes beside it, and the layer from x
   (projection + la_prefill on the activated outputs)
+* ``attention``: the softmax layer (partial RoPE + causal softmax attention) at B1 H64
+  N8192, TFLOP/s of the causal product against the measured bf16 peak
 * ``varlen``: a packed batch of 64K tokens in sequences of seeded lengths (1..8192)
   through ``la_prefill_varlen``, tokens/s and GB/s
 * ``e2e``: the same prefill with pinned host inputs, the H2D copies and the D2H
@@ -53,6 +55,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-varlen", action="store_true")
     ap.add_argument("--no-projection", action="store_true")
+    ap.add_argument("--no-attention", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -391,6 +394,9 @@ def run_ours(a):
     if not a.no_projection:
         line["projection"] = bench_projection(a, torch, la, WORKLOADS["proj_8k"], dev, stream,
                                               peaks, rank)
+    if not a.no_attention:
+        line["attention"] = bench_attention(a, torch, la, WORKLOADS["attn_8k"], dev, stream,
+                                            peaks, make_prefill_inputs, rank)
     if not a.no_varlen:
         line["varlen"] = bench_varlen(a, torch, la, WORKLOADS["prefill_varlen_64k"], dev,
                                       stream, peaks, make_prefill_inputs, rank)
@@ -495,6 +501,40 @@ def bench_projection(a, torch, la, w, dev, stream, peaks, rank):
             "cublas_ms": ms_cublas, "cublas_tflops": flops / (ms_cublas / 1e3) / 1e12,
             "layer_from_x_ms": ms_layer,
             "layer_from_x_tokens_per_s": w.N / (ms_layer / 1e3),
+            "gpu_launches_per_step": launches, "clocks": clk}
+
+
+def bench_attention(a, torch, la, w, dev, stream, peaks, make_prefill_inputs, rank):
+    """The softmax layer: one la_softmax_attention call per step (RoPE table, RoPE of q
+    and k, attention: three launches).  Algorithmic flops of the causal product:
+    2 d N (N + 1) per (sequence, head) for Q K^T and P V over the pairs s <= t."""
+    q, k, v, _ = make_prefill_inputs(w.B, w.N, w.H, w.d, torch.bfloat16, w.scale,
+                                     w.seed + 100 * rank, dev)
+    out = torch.empty_like(q)
+    steps = max(min(a.steps, 50), 10)
+
+    def step():
+        la.la_softmax_attention(q, k, v, out=out)
+
+    for _ in range(max(a.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if la.la_get_device_status() != 0:
+        raise SystemExit("device status error after the attention warm-up")
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    n0 = la.la_launch_count()
+    ms = sum(time_steps(torch, step, steps, stream)) / steps
+    launches = (la.la_launch_count() - n0) / steps
+    clk = clocks.stop()
+    flops = 2.0 * w.d * w.N * (w.N + 1) * w.H * w.B
+    tflops = flops / (ms / 1e3) / 1e12
+    del q, k, v, out
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "rope_base": 1.0e7,
+            "ms_per_step": ms, "tokens_per_s": w.B * w.N / (ms / 1e3), "tflops": tflops,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"],
+                         "kernel": "la_softmax_attention", "flops_per_step": flops},
             "gpu_launches_per_step": launches, "clocks": clk}
 
 

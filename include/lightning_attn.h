@@ -203,6 +203,29 @@ int la_get_device_status(void* cuda_stream);
 int la_qkvg_projection(const void* x, const void* w, void* q, void* k, void* v, void* g,
                        int64_t T, int hidden, int H, int d, unsigned flags, void* cuda_stream);
 
+/*
+ * The softmax layer of the hybrid stack: partial RoPE, then causal softmax attention.
+ * MiniMax-Text-01 puts one such layer after every seven Lightning Attention layers
+ * ("Hybrid Modeling", MiniMax-01 deep dive: RoPE on half of the head dimension); the
+ * model card's "Model Architecture" list gives 64 heads of size 128 and RoPE base
+ * 10,000,000.
+ *     q', k' = RoPE(q), RoPE(k): features [0, 64) of each head rotated as pairs
+ *              (i, i + 32) by the angle t * rope_base^(-i/32) at token t (t from 0 in
+ *              every sequence); features [64, 128) unchanged
+ *     out_t  = sum_{s <= t} softmax_s(q'_t . k'_s / sqrt(d)) v_s
+ *   q, k, v  in  [B][N][H][d] bf16 (one key/value head per query head)
+ *   out      out [B][N][H][d] bf16; must not overlap q, k or v
+ *   rope_base    > 1 (1e7 for MiniMax-Text-01)
+ * d must be 128 (LA_ERR_UNSUPPORTED otherwise), N <= 2^30; N = 0 does nothing.  The
+ * rotated copies of q and k and the cos/sin table live in the library's per-device
+ * workspace (grown on demand; 2 * B*N*H*d*2 + N*256 bytes).  Scores, the softmax and
+ * P*V run in fp32 with bf16 MMA operands; each output is rounded once to bf16.  Device
+ * pointers, 16-byte aligned, owned by the caller.  Argument errors are returned before
+ * any launch; a bounded device wait that gives up records LA_ERR_TIMEOUT.
+ */
+int la_softmax_attention(const void* q, const void* k, const void* v, void* out, int B, int H,
+                         int64_t N, int d, double rope_base, void* cuda_stream);
+
 /* Library version, major*10000 + minor*100 + patch. */
 int la_version(void);
 

@@ -22,7 +22,7 @@ import ctypes
 import os
 
 __all__ = ["la_prefill", "la_prefill_varlen", "la_decode_step", "la_decode_step_noalloc",
-           "la_qkvg_projection", "la_status_string", "la_get_device_status", "la_version",
+           "la_qkvg_projection", "la_softmax_attention", "la_status_string", "la_get_device_status", "la_version",
            "la_launch_count", "la_prefill_path", "LaError", "library_path", "load_library",
            "LA_BF16", "LA_F32", "LA_FLAG_SIMT", "LA_FLAG_ACTIVATED", "LA_PROJ_SILU"]
 
@@ -87,6 +87,9 @@ def load_library():
     lib.la_prefill_path.restype = i32
     lib.la_qkvg_projection.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, u32, vp]
     lib.la_qkvg_projection.restype = i32
+    lib.la_softmax_attention.argtypes = [vp, vp, vp, vp, i32, i32, i64, i32, ctypes.c_double,
+                                         vp]
+    lib.la_softmax_attention.restype = i32
     lib.la_launch_count.argtypes = []
     lib.la_launch_count.restype = ctypes.c_int64
     _lib = lib
@@ -258,6 +261,27 @@ def la_qkvg_projection(x, w, H: int, d: int = 128, activate: bool = True, out=No
         LA_PROJ_SILU if activate else 0, _stream_handle(stream))
     if rc != LA_OK:
         raise LaError(rc, "la_qkvg_projection")
+    return out
+
+
+def la_softmax_attention(q, k, v, out=None, rope_base: float = 1.0e7, stream=None):
+    """The softmax layer: RoPE on the first half of each head's features, then causal
+    softmax attention.  ``q, k, v``: bf16 ``[B, N, H, 128]`` (contiguous, CUDA).
+    Returns ``out`` of the same shape."""
+    import torch
+    B, N, H, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check([q, k, v, out], ["q", "k", "v", "out"])
+    for t, n in ((k, "k"), (v, "v"), (out, "out")):
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError(f"{n} must match q in shape and dtype")
+    if q.dtype != torch.bfloat16:
+        raise ValueError("la_softmax_attention takes bf16 tensors")
+    rc = load_library().la_softmax_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, N, d,
+                                             float(rope_base), _stream_handle(stream))
+    if rc != LA_OK:
+        raise LaError(rc, "la_softmax_attention")
     return out
 
 

@@ -1,0 +1,516 @@
+// la_attn_tc.cu -- the softmax layer of the hybrid stack on tensor cores (sm_103a):
+// partial RoPE, then causal softmax attention.
+//
+// What it computes.  MiniMax-Text-01 places one softmax attention layer after every
+// seven Lightning Attention layers ("Hybrid Modeling", MiniMax-01 deep dive); it
+// applies RoPE to half of the head dimension, with base frequency 10,000,000 (the
+// model card's "Model Architecture" list; 64 heads of size 128).  Here:
+//     q', k' = RoPE(q), RoPE(k):  features [0, 64) of a head rotated as pairs
+//              (i, i + 32), angle t * base^(-i/32) at token t; [64, 128) unchanged
+//     o_t    = sum_{s <= t} softmax_s(q'_t . k'_s / sqrt(d)) v_s
+// with q, k, v, o laid out [B][N][H][d] bf16 like the linear layer's tensors.
+//
+// Design:
+//  * k_rope_table writes cos/sin of every (token, pair) angle in fp32, each computed
+//    in fp64 (angles reach 1e6 rad at 1M tokens).  k_rope rotates q and k into
+//    library-owned copies (one RNE rounding to bf16).
+//  * k_attn_fwd: one CTA per (128-query tile, head, sequence), the tiles with the most
+//    key tiles first.  Warp 0 lane 0 loads the query tile once and the key/value
+//    tiles of the causal range into two stages by TMA (128B swizzle).  Warp 1 lane 0
+//    issues tcgen05 MMAs: S_j = Q K_j^T (128 x 128, fp32) into one of two TMEM score
+//    buffers, and O += P_j V_j (P in TMEM, bf16) as two 64-column halves.  Warps 4-7
+//    own one query row per thread: they read S_j from TMEM, mask it (causal, keys past
+//    N), keep the running max m and sum l of the online softmax in base 2, write P_j
+//    as bf16 over the first 64 columns of its score buffer, and rescale O in TMEM when
+//    a row's max moved.  The QK product of the next key tile runs while the softmax
+//    works on this one.  At the end they divide O by l and store bf16 rows.
+//  * Every wait is bounded (%globaltimer); a CTA that gives up records LA_ERR_TIMEOUT
+//    in the status word, lets its copies and MMAs finish, frees TMEM and exits.
+//
+// TMEM columns: [0, 128) S_0 / P_0 | [128, 256) S_1 / P_1 | [256, 384) O.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "../../include/lightning_attn.h"
+#include "la_internal.h"
+#include "la_sm100.cuh"
+
+namespace la {
+namespace {
+
+using namespace sm100;
+
+constexpr int D = kHeadDim;            // 128
+constexpr int BQ = 128;                // queries per tile (TMEM lanes)
+constexpr int BKV = 128;               // keys per tile
+constexpr int kPairs = D / 4;          // rotated pairs: features [0, 64) of a head
+constexpr int kThreads = 256;          // 8 warps
+constexpr uint32_t HALF = 16384;       // 128 rows x 64 bf16, one 128B-swizzled block
+constexpr uint32_t TILE = 2 * HALF;    // 128 rows x 128 bf16
+constexpr uint32_t OFF_Q = 0;
+constexpr uint32_t OFF_K = OFF_Q + TILE;        // 2 stages
+constexpr uint32_t OFF_V = OFF_K + 2 * TILE;    // 2 stages
+constexpr uint32_t SMEM_USED = OFF_V + 2 * TILE;      // 160 KiB
+constexpr uint32_t SMEM_DYN = SMEM_USED + 1024;       // + alignment slack
+static_assert(SMEM_DYN + 1024 <= 227 * 1024, "shared memory budget");
+constexpr uint32_t TM_S = 0, TM_O = 256;
+constexpr uint32_t IDESC_S = idesc_bf16_f32(BQ, BKV, 0, 0);   // Q K-major, K K-major
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(BQ, 64, 0, 1);   // P (TMEM), V MN-major
+constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s
+constexpr uint64_t kDrainNs = 200000000ull;     // 0.2 s
+
+struct AttnParams {
+    __nv_bfloat16* out;
+    int* status;
+    int B, H, N;
+    int Qt;            // query tiles per sequence
+    float scale_log2;  // log2(e) / sqrt(d)
+};
+
+struct Shared {
+    uint64_t qfull, kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], pfull[2], pvdone,
+        mmadone;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ bool abort_set(Shared& sh) {
+    return *reinterpret_cast<volatile int*>(&sh.abort_flag) != 0;
+}
+// Bounded wait for the phase of `bar` with `parity`; false when the CTA is aborting
+// (honor_abort) or after `limit_ns`, in which case it raises the abort itself.
+__device__ bool wait_bar(Shared& sh, int* status, uint64_t* bar, uint32_t parity,
+                         bool honor_abort = true, uint64_t limit_ns = kTimeoutNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 15u) == 0) {
+            if (honor_abort && abort_set(sh)) return false;
+            if (global_timer_ns() - t0 > limit_ns) {
+                *reinterpret_cast<volatile int*>(&sh.abort_flag) = 1;
+                atomicExch(status, LA_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Smem descriptors (128B swizzle).  K-major operand of 128 x 128 bf16 stored as two
+// 64-wide halves; k-step ks (16 elements = 32 bytes).  MN-major operand (rows = K,
+// one 64-wide MN block): k-step ks covers 16 rows (2048 bytes).
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int ks) {
+    return smem_desc_sw128(base + (ks >> 2) * HALF + (ks & 3) * 32, 16, 1024);
+}
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int ks) {
+    return smem_desc_sw128(base + ks * 2048, HALF, 1024);
+}
+
+// ------------------------------------------------------------------ RoPE
+// cs[t][i] = (cos, sin) of t * base^(-i / kPairs), the angle and both functions in fp64.
+__global__ void k_rope_table(float2* __restrict__ cs, int N, double base) {
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= static_cast<int64_t>(N) * kPairs) return;
+    const int t = static_cast<int>(idx / kPairs), i = static_cast<int>(idx % kPairs);
+    const double ang = static_cast<double>(t) * pow(base, -static_cast<double>(i) / kPairs);
+    double s, c;
+    sincos(ang, &s, &c);
+    cs[idx] = make_float2(static_cast<float>(c), static_cast<float>(s));
+}
+
+// One warp per (token, head) row of q (blockIdx.y = 0) or k (1); rows are [B][N][H]:
+// lane l rotates the pair (l, l + 32) by the row's token angle and copies features
+// 64 + l and 96 + l.
+__global__ void k_rope(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                       __nv_bfloat16* __restrict__ qr, __nv_bfloat16* __restrict__ kr,
+                       const float2* __restrict__ cs, int64_t rows, int H, int N) {
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+    if (row >= rows) return;
+    const int lane = threadIdx.x & 31;
+    const __nv_bfloat16* src = (blockIdx.y == 0 ? q : k) + row * D;
+    __nv_bfloat16* dst = (blockIdx.y == 0 ? qr : kr) + row * D;
+    const int64_t t = (row / H) % N;  // token position within its sequence
+    const float2 r = cs[t * kPairs + lane];
+    const float a = __bfloat162float(src[lane]), b = __bfloat162float(src[lane + 32]);
+    dst[lane] = __float2bfloat16_rn(a * r.x - b * r.y);
+    dst[lane + 32] = __float2bfloat16_rn(a * r.y + b * r.x);
+    dst[64 + lane] = src[64 + lane];
+    dst[96 + lane] = src[96 + lane];
+}
+
+// ------------------------------------------------------------------ attention
+__global__ void __launch_bounds__(kThreads, 1)
+    k_attn_fwd(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap tv, const AttnParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ Shared sh;
+    uint8_t* sm = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int BH = p.B * p.H;
+    const int qi = p.Qt - 1 - static_cast<int>(blockIdx.x / BH);  // most key tiles first
+    const int bh = static_cast<int>(blockIdx.x % BH);
+    const int b = bh / p.H, h = bh - (bh / p.H) * p.H;
+    const int nkv = qi + 1;  // causal: key tiles 0 .. qi
+
+    if (tid == 0) {
+        mbar_init(&sh.qfull, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&sh.kfull[s], 1);
+            mbar_init(&sh.kempty[s], 1);
+            mbar_init(&sh.vfull[s], 1);
+            mbar_init(&sh.vempty[s], 1);
+            mbar_init(&sh.sfull[s], 1);
+            mbar_init(&sh.pfull[s], 4);  // one arrival per softmax warp
+        }
+        mbar_init(&sh.pvdone, 1);
+        mbar_init(&sh.mmadone, 1);
+        sh.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 2) tmem_alloc(&sh.tmem_base, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = sh.tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------------------ TMA producer
+            const int col = h * D;
+            mbar_arrive_expect_tx(&sh.qfull, TILE);
+            tma_load_3d(sm + OFF_Q, &tq, col, qi * BQ, b, &sh.qfull);
+            tma_load_3d(sm + OFF_Q + HALF, &tq, col + 64, qi * BQ, b, &sh.qfull);
+            int issued = 0;
+            for (int j = 0; j < nkv; ++j) {
+                const int s = j & 1;
+                const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
+                if (!wait_bar(sh, p.status, &sh.kempty[s], ph ^ 1u)) break;
+                mbar_arrive_expect_tx(&sh.kfull[s], TILE);
+                tma_load_3d(sm + OFF_K + s * TILE, &tk, col, j * BKV, b, &sh.kfull[s]);
+                tma_load_3d(sm + OFF_K + s * TILE + HALF, &tk, col + 64, j * BKV, b, &sh.kfull[s]);
+                if (!wait_bar(sh, p.status, &sh.vempty[s], ph ^ 1u)) {
+                    issued = -(j + 1);  // K_j issued, V_j not
+                    break;
+                }
+                mbar_arrive_expect_tx(&sh.vfull[s], TILE);
+                tma_load_3d(sm + OFF_V + s * TILE, &tv, col, j * BKV, b, &sh.vfull[s]);
+                tma_load_3d(sm + OFF_V + s * TILE + HALF, &tv, col + 64, j * BKV, b, &sh.vfull[s]);
+                issued = j + 1;
+            }
+            // drain: every load issued lands before this CTA may exit
+            wait_bar(sh, p.status, &sh.qfull, 0, false, kDrainNs);
+            const int nk = issued < 0 ? -issued : issued;   // K tiles issued
+            const int nv = issued < 0 ? -issued - 1 : issued;
+            for (int j = nk - 2 < 0 ? 0 : nk - 2; j < nk; ++j)
+                wait_bar(sh, p.status, &sh.kfull[j & 1], static_cast<uint32_t>(j >> 1) & 1u,
+                         false, kDrainNs);
+            for (int j = nv - 2 < 0 ? 0 : nv - 2; j < nv; ++j)
+                wait_bar(sh, p.status, &sh.vfull[j & 1], static_cast<uint32_t>(j >> 1) & 1u,
+                         false, kDrainNs);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------------------ MMA issuer
+            const uint32_t qa = sbase + OFF_Q;
+            bool ok = wait_bar(sh, p.status, &sh.qfull, 0);
+            // S_j = Q K_j^T into score buffer j & 1
+            auto issue_qk = [&](int j) -> bool {
+                const int s = j & 1;
+                if (!wait_bar(sh, p.status, &sh.kfull[s], static_cast<uint32_t>(j >> 1) & 1u))
+                    return false;
+                tc_fence_after();
+                const uint32_t ka = sbase + OFF_K + s * TILE;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+                    mma_ss(tm + TM_S + s * BKV, desc_kmajor(qa, ks), desc_kmajor(ka, ks), IDESC_S,
+                           ks > 0 ? 1u : 0u);
+                mma_commit(&sh.kempty[s]);
+                mma_commit(&sh.sfull[s]);
+                return true;
+            };
+            if (ok) ok = issue_qk(0);
+            for (int j = 0; j < nkv && ok; ++j) {
+                const int s = j & 1;
+                const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
+                if (j + 1 < nkv) {
+                    // score buffer (j + 1) & 1 holds P_{j-1} until PV_{j-1} is done
+                    if (j >= 1 && !wait_bar(sh, p.status, &sh.pvdone,
+                                            static_cast<uint32_t>(j - 1) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!issue_qk(j + 1)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (!wait_bar(sh, p.status, &sh.pfull[s], ph) ||
+                    !wait_bar(sh, p.status, &sh.vfull[s], ph)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t va = sbase + OFF_V + s * TILE;
+#pragma unroll
+                for (int half = 0; half < 2; ++half)
+#pragma unroll
+                    for (int ks = 0; ks < BKV / 16; ++ks)
+                        mma_ts(tm + TM_O + 64 * half, tm + TM_S + s * BKV + ks * 8,
+                               desc_mnmajor(va + half * HALF, ks), IDESC_PV,
+                               (j > 0 || ks > 0) ? 1u : 0u);
+                mma_commit(&sh.vempty[s]);
+                mma_commit(&sh.pvdone);
+            }
+            mma_commit(&sh.mmadone);
+            wait_bar(sh, p.status, &sh.mmadone, 0, false, kDrainNs);
+        }
+    } else if (warp >= 4) {
+        // ---------------------------------------------------------------- softmax rows
+        const int quarter = warp & 3;              // TMEM lanes 32 quarter .. + 31
+        const int r = quarter * 32 + lane;         // query row of the tile
+        const int qrow = qi * BQ + r;              // token position
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        float m = -INFINITY, l = 0.0f;
+        bool ok = true;
+        for (int j = 0; j < nkv; ++j) {
+            const int s = j & 1;
+            const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
+            if (!__all_sync(0xffffffffu, wait_bar(sh, p.status, &sh.sfull[s], ph))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t sa = tm + TM_S + s * BKV + lane_off;
+            float x[BKV];
+#pragma unroll
+            for (int c = 0; c < BKV / 32; ++c) {
+                uint32_t u[32];
+                LA_TMEM_LD32(sa + c * 32, u);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(u[e]);
+            }
+            // scores in base 2; keys after the query or past N are masked
+            const int k0 = j * BKV;
+            const int kmax = min(qrow, p.N - 1) - k0;  // last allowed key of this tile
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < BKV; ++c) {
+                const float t = c <= kmax ? x[c] * p.scale_log2 : -INFINITY;
+                x[c] = t;
+                mx = fmaxf(mx, t);
+            }
+            const float m_new = fmaxf(m, mx);
+            const float m_use = m_new == -INFINITY ? 0.0f : m_new;  // a row with no key yet
+            const float alpha = ex2_approx(m - m_use);
+            float sum = 0.0f;
+            uint32_t pk[BKV / 2];
+#pragma unroll
+            for (int c = 0; c < BKV / 2; ++c) {
+                const float p0 = ex2_approx(x[2 * c] - m_use);
+                const float p1 = ex2_approx(x[2 * c + 1] - m_use);
+                sum += p0 + p1;
+                pk[c] = pack_bf16x2(p0, p1);
+            }
+            l = l * alpha + sum;
+            m = m_new;
+            LA_TMEM_ST32(sa, pk);
+            LA_TMEM_ST32(sa + 32, (pk + 32));
+            tmem_wait_st();
+            if (j > 0) {
+                // O holds PV_{j-1} once it is done; rescale rows whose max moved
+                if (!__all_sync(0xffffffffu,
+                                wait_bar(sh, p.status, &sh.pvdone,
+                                         static_cast<uint32_t>(j - 1) & 1u))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+                    const uint32_t oa = tm + TM_O + lane_off;
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t u[32];
+                        LA_TMEM_LD32(oa + c * 32, u);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
+                        LA_TMEM_ST32(oa + c * 32, u);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.pfull[s]);
+        }
+        // ------------------------------------------------------------ epilogue
+        if (ok && __all_sync(0xffffffffu, wait_bar(sh, p.status, &sh.pvdone,
+                                                    static_cast<uint32_t>(nkv - 1) & 1u))) {
+            tc_fence_after();
+            const float inv = 1.0f / l;
+            const uint32_t oa = tm + TM_O + lane_off;
+            __nv_bfloat16* dst =
+                p.out + ((static_cast<int64_t>(b) * p.N + qrow) * p.H + h) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t u[32];
+                LA_TMEM_LD32(oa + c * 32, u);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = pack_bf16x2(__uint_as_float(u[2 * e]) * inv,
+                                        __uint_as_float(u[2 * e + 1]) * inv);
+                if (qrow < p.N) {
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 2) tmem_dealloc(tm, 512);
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+std::mutex g_attr_mutex;
+bool g_attr_set[64];  // per device: the kernel's shared-memory attribute is set
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        else
+            cudaGetLastError();
+    });
+    return g_encode;
+}
+
+// [B][N][H*d] bf16 as a 3-D tensor (feature, token, sequence), boxes of 64 features x
+// 128 tokens, 128B swizzle; reads past N give zeros.
+bool encode_io_map(CUtensorMap* m, const void* base, int B, int H, int64_t N) {
+    auto enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(H) * D, static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(H) * D * 2,
+                             static_cast<cuuint64_t>(N) * H * D * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool prepare_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    std::lock_guard<std::mutex> lock(g_attr_mutex);
+    if (!g_attr_set[dev]) {
+        if (cudaFuncSetAttribute(k_attn_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(SMEM_DYN)) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        g_attr_set[dev] = true;
+    }
+    return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+}  // namespace
+}  // namespace la
+
+using namespace la;
+
+extern "C" int la_softmax_attention(const void* q, const void* k, const void* v, void* out,
+                                    int B, int H, int64_t N, int d, double rope_base,
+                                    void* cuda_stream) {
+    if (B <= 0 || H <= 0 || N < 0 || d <= 0) return LA_ERR_INVALID_ARG;
+    if (!(rope_base > 1.0) || !isfinite(rope_base)) return LA_ERR_INVALID_ARG;
+    if (d != D) return LA_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !out) return LA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, out};
+    for (const void* x : ptrs)
+        if (!aligned16(x)) return LA_ERR_MISALIGNED;
+    if (N > (int64_t(1) << 30)) return LA_ERR_UNSUPPORTED;
+    const int64_t Qt = (N + BQ - 1) / BQ;
+    if (Qt * B * H > (int64_t(1) << 31) - 1 || static_cast<int64_t>(B) * H > (1 << 24))
+        return LA_ERR_UNSUPPORTED;
+    const size_t bytes = static_cast<size_t>(B) * N * H * D * 2;
+    if (overlaps(out, bytes, q, bytes) || overlaps(out, bytes, k, bytes) ||
+        overlaps(out, bytes, v, bytes))
+        return LA_ERR_INVALID_ARG;
+    if (N == 0) return LA_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
+    if (!prepare_device()) return LA_ERR_CUDA;
+    // workspace: rotated q and k (bf16), then the cos/sin table
+    const size_t table_bytes = static_cast<size_t>(N) * kPairs * sizeof(float2);
+    Workspace ws;
+    int rc = workspace_acquire(2 * bytes + table_bytes, st, &ws);
+    if (rc != LA_OK) return rc;
+    auto* qr = static_cast<__nv_bfloat16*>(ws.base);
+    auto* kr = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws.base) + bytes);
+    auto* cs = reinterpret_cast<float2*>(static_cast<char*>(ws.base) + 2 * bytes);
+    const int64_t nt = N * kPairs;
+    k_rope_table<<<static_cast<unsigned>((nt + 255) / 256), 256, 0, st>>>(cs, static_cast<int>(N),
+                                                                         rope_base);
+    const int64_t rows = static_cast<int64_t>(B) * N * H;
+    k_rope<<<dim3(static_cast<unsigned>((rows + 7) / 8), 2), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), qr, kr, cs,
+        rows, H, static_cast<int>(N));
+    CUtensorMap mq, mk, mv;
+    if (!encode_io_map(&mq, qr, B, H, N) || !encode_io_map(&mk, kr, B, H, N) ||
+        !encode_io_map(&mv, v, B, H, N))
+        return LA_ERR_UNSUPPORTED;
+    AttnParams prm;
+    prm.out = static_cast<__nv_bfloat16*>(out);
+    prm.status = ws.status;
+    prm.B = B;
+    prm.H = H;
+    prm.N = static_cast<int>(N);
+    prm.Qt = static_cast<int>(Qt);
+    prm.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(D)));
+    k_attn_fwd<<<static_cast<unsigned>(Qt * B * H), kThreads, SMEM_DYN, st>>>(mq, mk, mv, prm);
+    if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
+    note_launches(3);
+    return LA_OK;
+}

@@ -41,6 +41,8 @@ WORKLOADS = {
     "prefill_1m": Workload("prefill_1m", 1, 64, 1048576, 128, "bf16", 0.5, 5),
     # input projection of the 8K prefill: x [8192, 6144] -> q, k, v, g [8192, 64, 128]
     "proj_8k": Workload("proj_8k", 1, 64, 8192, 128, "bf16", 1.0, 7, hidden=6144),
+    # the softmax layer at the 8K prefill's shape: q, k, v N(0,1), RoPE base 1e7
+    "attn_8k": Workload("attn_8k", 1, 64, 8192, 128, "bf16", 1.0, 8),
     # packed batch: 64K tokens in sequences of seeded lengths (varlen_lengths)
     "prefill_varlen_64k": Workload("prefill_varlen_64k", 1, 64, 65536, 128, "bf16", 0.5, 6),
 }

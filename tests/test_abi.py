@@ -38,6 +38,7 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     for want in ["la_prefill", "la_decode_step", "la_prefill_ex", "la_decode_step_ex",
                  "la_prefill_varlen", "la_prefill_varlen_ex", "la_qkvg_projection",
+                 "la_softmax_attention",
                  "la_status_string", "la_get_device_status", "la_version", "la_launch_count",
                  "la_prefill_path"]:
         assert want in names
@@ -190,4 +191,32 @@ def test_projection_rejects_on_host(lib, kw, want):
 def test_projection_empty_batch_launches_nothing(lib):
     n0 = lib.la_launch_count()
     assert _proj(lib, T=0) == la.LA_OK
+    assert lib.la_launch_count() == n0
+
+
+def _attn(lib, B=1, H=2, N=16, d=128, base=1e7, q=None, out=None):
+    return lib.la_softmax_attention(q if q is not None else P[0], P[1], P[2],
+                                    out if out is not None else P[3], B, H, N, d, base, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(B=0), la.LA_ERR_INVALID_ARG),
+    (dict(H=-1), la.LA_ERR_INVALID_ARG),
+    (dict(N=-1), la.LA_ERR_INVALID_ARG),
+    (dict(d=64), la.LA_ERR_UNSUPPORTED),
+    (dict(base=1.0), la.LA_ERR_INVALID_ARG),
+    (dict(base=float("inf")), la.LA_ERR_INVALID_ARG),
+    (dict(base=float("nan")), la.LA_ERR_INVALID_ARG),
+    (dict(q=ctypes.c_void_p(0)), la.LA_ERR_INVALID_ARG),
+    (dict(q=MIS), la.LA_ERR_MISALIGNED),
+    (dict(out=P[1]), la.LA_ERR_INVALID_ARG),           # out aliases k
+    (dict(N=(1 << 30) + 1), la.LA_ERR_UNSUPPORTED),
+])
+def test_softmax_attention_rejects_on_host(lib, kw, want):
+    assert _attn(lib, **kw) == want
+
+
+def test_softmax_attention_empty_launches_nothing(lib):
+    n0 = lib.la_launch_count()
+    assert _attn(lib, N=0) == la.LA_OK
     assert lib.la_launch_count() == n0
