@@ -165,9 +165,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_addr(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int BH = p.B * p.H;
-    const int qi = p.Qt - 1 - static_cast<int>(blockIdx.x / BH);  // most key tiles first
-    const int bh = static_cast<int>(blockIdx.x % BH);
+    // head-major order, the query tiles of a head with the most key tiles first: CTAs
+    // running together share their heads' key/value tiles in L2
+    const int bh = static_cast<int>(blockIdx.x / p.Qt);
+    const int qi = p.Qt - 1 - static_cast<int>(blockIdx.x % p.Qt);
     const int b = bh / p.H, h = bh - (bh / p.H) * p.H;
     const int nkv = qi + 1;  // causal: key tiles 0 .. qi
 
@@ -300,38 +301,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const uint32_t sa = tm + TM_S + s * BKV + lane_off;
-            float x[BKV];
+            uint32_t xu[BKV];
 #pragma unroll
-            for (int c = 0; c < BKV / 32; ++c) {
-                uint32_t u[32];
-                LA_TMEM_LD32(sa + c * 32, u);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(u[e]);
-            }
-            // scores in base 2; keys after the query or past N are masked
+            for (int c = 0; c < BKV / 32; ++c) LA_TMEM_LD32(sa + c * 32, (xu + c * 32));
+            tmem_wait_ld();
+            // keys after the query or past N are masked; a tile below the diagonal and
+            // inside N (the same for every row of the tile) needs no mask
             const int k0 = j * BKV;
-            const int kmax = min(qrow, p.N - 1) - k0;  // last allowed key of this tile
-            float mx = -INFINITY;
+            if (!(j < qi && k0 + BKV <= p.N)) {
+                const int kmax = min(qrow, p.N - 1) - k0;  // last allowed key of this tile
 #pragma unroll
-            for (int c = 0; c < BKV; ++c) {
-                const float t = c <= kmax ? x[c] * p.scale_log2 : -INFINITY;
-                x[c] = t;
-                mx = fmaxf(mx, t);
+                for (int c = 0; c < BKV; ++c)
+                    if (c > kmax) xu[c] = __float_as_uint(-INFINITY);
             }
-            const float m_new = fmaxf(m, mx);
+            // the row max on raw scores (the scale is positive), four chains
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int c = 0; c < BKV; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], __uint_as_float(xu[c]));
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            const float m_new = fmaxf(m, mx * p.scale_log2);   // base-2 units
             const float m_use = m_new == -INFINITY ? 0.0f : m_new;  // a row with no key yet
             const float alpha = ex2_approx(m - m_use);
-            float sum = 0.0f;
+            float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
             uint32_t pk[BKV / 2];
 #pragma unroll
             for (int c = 0; c < BKV / 2; ++c) {
-                const float p0 = ex2_approx(x[2 * c] - m_use);
-                const float p1 = ex2_approx(x[2 * c + 1] - m_use);
-                sum += p0 + p1;
+                const float p0 = ex2_approx(fmaf(__uint_as_float(xu[2 * c]), p.scale_log2, -m_use));
+                const float p1 =
+                    ex2_approx(fmaf(__uint_as_float(xu[2 * c + 1]), p.scale_log2, -m_use));
+                sum4[c & 3] += p0 + p1;
                 pk[c] = pack_bf16x2(p0, p1);
             }
-            l = l * alpha + sum;
+            l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
             m = m_new;
             LA_TMEM_ST32(sa, pk);
             LA_TMEM_ST32(sa + 32, (pk + 32));
