@@ -14,20 +14,23 @@
 //  * k_rope_table writes cos/sin of every (token, pair) angle in fp32, each computed
 //    in fp64 (angles reach 1e6 rad at 1M tokens).  k_rope rotates q and k into
 //    library-owned copies (one RNE rounding to bf16).
-//  * k_attn_fwd: one CTA per (128-query tile, head, sequence), the tiles with the most
-//    key tiles first.  Warp 0 lane 0 loads the query tile once and the key/value
-//    tiles of the causal range into two stages by TMA (128B swizzle).  Warp 1 lane 0
-//    issues tcgen05 MMAs: S_j = Q K_j^T (128 x 128, fp32) into one of two TMEM score
-//    buffers, and O += P_j V_j (P in TMEM, bf16) as two 64-column halves.  Warps 4-7
-//    own one query row per thread: they read S_j from TMEM, mask it (causal, keys past
-//    N), keep the running max m and sum l of the online softmax in base 2, write P_j
-//    as bf16 over the first 64 columns of its score buffer, and rescale O in TMEM when
-//    a row's max moved.  The QK product of the next key tile runs while the softmax
-//    works on this one.  At the end they divide O by l and store bf16 rows.
+//  * k_attn_fwd: one CTA per (pair of 128-query tiles, head, sequence), head-major,
+//    the pairs with the most key tiles first.  Warp 0 lane 0 loads both query tiles
+//    once and the key/value tiles of the causal range into two stages by TMA (128B
+//    swizzle); the two query tiles share every key/value tile.  Warp 1 lane 0 issues
+//    tcgen05 MMAs: S_t = Q_t K_j^T (128 x 128, fp32) into query tile t's TMEM score
+//    buffer, and O_t += P_t V_j (P in TMEM, bf16) as two 64-column halves, followed at
+//    once by S_t of the next key tile.  Warps 4-7 (tile 0) and 8-11 (tile 1) own one
+//    query row per thread: they read S_t from TMEM, mask it (causal, keys past N),
+//    keep the running max m and sum l of the online softmax in base 2, write P_t as
+//    bf16 over the first 64 columns of the score buffer, and rescale O_t in TMEM when
+//    a row's max moved.  While one tile's softmax runs, the tensor pipe works on the
+//    other tile.  At the end they divide O_t by l and store bf16 rows.
 //  * Every wait is bounded (%globaltimer); a CTA that gives up records LA_ERR_TIMEOUT
 //    in the status word, lets its copies and MMAs finish, frees TMEM and exits.
 //
-// TMEM columns: [0, 128) S_0 / P_0 | [128, 256) S_1 / P_1 | [256, 384) O.
+// TMEM columns: [0, 128) S / P of query tile 0 | [128, 256) of tile 1 |
+//               [256, 384) O of tile 0 | [384, 512) O of tile 1.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -50,18 +53,19 @@ constexpr int D = kHeadDim;            // 128
 constexpr int BQ = 128;                // queries per tile (TMEM lanes)
 constexpr int BKV = 128;               // keys per tile
 constexpr int kPairs = D / 4;          // rotated pairs: features [0, 64) of a head
-constexpr int kThreads = 256;          // 8 warps
+constexpr int kThreads = 384;          // 12 warps
 constexpr uint32_t HALF = 16384;       // 128 rows x 64 bf16, one 128B-swizzled block
 constexpr uint32_t TILE = 2 * HALF;    // 128 rows x 128 bf16
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = OFF_Q + TILE;        // 2 stages
+constexpr uint32_t OFF_Q = 0;                   // 2 query tiles
+constexpr uint32_t OFF_K = OFF_Q + 2 * TILE;    // 2 stages
 constexpr uint32_t OFF_V = OFF_K + 2 * TILE;    // 2 stages
-constexpr uint32_t SMEM_USED = OFF_V + 2 * TILE;      // 160 KiB
+constexpr uint32_t SMEM_USED = OFF_V + 2 * TILE;      // 192 KiB
 constexpr uint32_t SMEM_DYN = SMEM_USED + 1024;       // + alignment slack
 static_assert(SMEM_DYN + 1024 <= 227 * 1024, "shared memory budget");
 constexpr uint32_t TM_S = 0, TM_O = 256;
 constexpr uint32_t IDESC_S = idesc_bf16_f32(BQ, BKV, 0, 0);   // Q K-major, K K-major
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(BQ, 64, 0, 1);   // P (TMEM), V MN-major
+constexpr float kMaxSlack = 8.0f;      // base-2 growth of a row's max before O rescales
 constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s
 constexpr uint64_t kDrainNs = 200000000ull;     // 0.2 s
 
@@ -70,11 +74,13 @@ struct AttnParams {
     int* status;
     int B, H, N;
     int Qt;            // query tiles per sequence
+    int Qp;            // pairs of query tiles per sequence (a CTA each)
     float scale_log2;  // log2(e) / sqrt(d)
 };
 
 struct Shared {
-    uint64_t qfull, kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], pfull[2], pvdone,
+    // sfull, pfull, pvdone: one per query tile of the pair
+    uint64_t qfull, kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], pfull[2], pvdone[2],
         mmadone;
     uint32_t tmem_base;
     int abort_flag;
@@ -165,12 +171,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_addr(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // head-major order, the query tiles of a head with the most key tiles first: CTAs
+    // head-major order, the tile pairs of a head with the most key tiles first: CTAs
     // running together share their heads' key/value tiles in L2
-    const int bh = static_cast<int>(blockIdx.x / p.Qt);
-    const int qi = p.Qt - 1 - static_cast<int>(blockIdx.x % p.Qt);
+    const int bh = static_cast<int>(blockIdx.x / p.Qp);
+    const int q0 = 2 * (p.Qp - 1 - static_cast<int>(blockIdx.x % p.Qp));  // first query tile
     const int b = bh / p.H, h = bh - (bh / p.H) * p.H;
-    const int nkv = qi + 1;  // causal: key tiles 0 .. qi
+    const int ntile = q0 + 1 < p.Qt ? 2 : 1;
+    const int nkv = q0 + ntile;  // causal: key tiles 0 .. q0 + ntile - 1
 
     if (tid == 0) {
         mbar_init(&sh.qfull, 1);
@@ -180,9 +187,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.vfull[s], 1);
             mbar_init(&sh.vempty[s], 1);
             mbar_init(&sh.sfull[s], 1);
-            mbar_init(&sh.pfull[s], 4);  // one arrival per softmax warp
+            mbar_init(&sh.pfull[s], 4);  // one arrival per softmax warp of the tile
+            mbar_init(&sh.pvdone[s], 1);
         }
-        mbar_init(&sh.pvdone, 1);
         mbar_init(&sh.mmadone, 1);
         sh.abort_flag = 0;
         fence_mbar_init();
@@ -197,9 +204,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // ------------------------------------------------------------ TMA producer
             const int col = h * D;
-            mbar_arrive_expect_tx(&sh.qfull, TILE);
-            tma_load_3d(sm + OFF_Q, &tq, col, qi * BQ, b, &sh.qfull);
-            tma_load_3d(sm + OFF_Q + HALF, &tq, col + 64, qi * BQ, b, &sh.qfull);
+            mbar_arrive_expect_tx(&sh.qfull, ntile * TILE);
+            for (int t = 0; t < ntile; ++t) {
+                tma_load_3d(sm + OFF_Q + t * TILE, &tq, col, (q0 + t) * BQ, b, &sh.qfull);
+                tma_load_3d(sm + OFF_Q + t * TILE + HALF, &tq, col + 64, (q0 + t) * BQ, b,
+                            &sh.qfull);
+            }
             int issued = 0;
             for (int j = 0; j < nkv; ++j) {
                 const int s = j & 1;
@@ -231,123 +241,150 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------------------ MMA issuer
-            const uint32_t qa = sbase + OFF_Q;
+            // Query tile t, key tile j: S_t = Q_t K_j^T into t's score buffer; once t's
+            // softmax has written P_t there, O_t += P_t V_j, and right after that product
+            // S_t for key tile j + 1.  While one tile's softmax runs, the tensor pipe
+            // works on the other tile.
             bool ok = wait_bar(sh, p.status, &sh.qfull, 0);
-            // S_j = Q K_j^T into score buffer j & 1
-            auto issue_qk = [&](int j) -> bool {
-                const int s = j & 1;
-                if (!wait_bar(sh, p.status, &sh.kfull[s], static_cast<uint32_t>(j >> 1) & 1u))
-                    return false;
-                tc_fence_after();
-                const uint32_t ka = sbase + OFF_K + s * TILE;
+            auto issue_s = [&](int t, int j) {
+                const uint32_t qa = sbase + OFF_Q + t * TILE;
+                const uint32_t ka = sbase + OFF_K + (j & 1) * TILE;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
-                    mma_ss(tm + TM_S + s * BKV, desc_kmajor(qa, ks), desc_kmajor(ka, ks), IDESC_S,
+                    mma_ss(tm + TM_S + t * BKV, desc_kmajor(qa, ks), desc_kmajor(ka, ks), IDESC_S,
                            ks > 0 ? 1u : 0u);
-                mma_commit(&sh.kempty[s]);
-                mma_commit(&sh.sfull[s]);
-                return true;
+                mma_commit(&sh.sfull[t]);
             };
-            if (ok) ok = issue_qk(0);
+            if (ok) ok = wait_bar(sh, p.status, &sh.kfull[0], 0);
+            if (ok) {
+                tc_fence_after();
+                for (int t = 0; t < ntile; ++t) issue_s(t, 0);
+                mma_commit(&sh.kempty[0]);
+            }
             for (int j = 0; j < nkv && ok; ++j) {
                 const int s = j & 1;
-                const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
-                if (j + 1 < nkv) {
-                    // score buffer (j + 1) & 1 holds P_{j-1} until PV_{j-1} is done
-                    if (j >= 1 && !wait_bar(sh, p.status, &sh.pvdone,
-                                            static_cast<uint32_t>(j - 1) & 1u)) {
-                        ok = false;
-                        break;
-                    }
-                    if (!issue_qk(j + 1)) {
-                        ok = false;
-                        break;
-                    }
-                }
-                if (!wait_bar(sh, p.status, &sh.pfull[s], ph) ||
-                    !wait_bar(sh, p.status, &sh.vfull[s], ph)) {
+                if (!wait_bar(sh, p.status, &sh.vfull[s], static_cast<uint32_t>(j >> 1) & 1u)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
                 const uint32_t va = sbase + OFF_V + s * TILE;
+                const bool next = j + 1 < nkv;
+                if (next && !wait_bar(sh, p.status, &sh.kfull[(j + 1) & 1],
+                                      static_cast<uint32_t>((j + 1) >> 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                for (int t = 0; t < ntile && ok; ++t) {
+                    if (j > q0 + t) continue;  // past tile t's causal range
+                    if (!wait_bar(sh, p.status, &sh.pfull[t], static_cast<uint32_t>(j) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll
-                for (int half = 0; half < 2; ++half)
+                    for (int half = 0; half < 2; ++half)
 #pragma unroll
-                    for (int ks = 0; ks < BKV / 16; ++ks)
-                        mma_ts(tm + TM_O + 64 * half, tm + TM_S + s * BKV + ks * 8,
-                               desc_mnmajor(va + half * HALF, ks), IDESC_PV,
-                               (j > 0 || ks > 0) ? 1u : 0u);
+                        for (int ks = 0; ks < BKV / 16; ++ks)
+                            mma_ts(tm + TM_O + t * BKV + 64 * half, tm + TM_S + t * BKV + ks * 8,
+                                   desc_mnmajor(va + half * HALF, ks), IDESC_PV,
+                                   (j > 0 || ks > 0) ? 1u : 0u);
+                    mma_commit(&sh.pvdone[t]);
+                    if (j + 1 <= q0 + t) {
+                        // the score buffer holds P_t until this product is done
+                        if (!wait_bar(sh, p.status, &sh.pvdone[t], static_cast<uint32_t>(j) & 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_s(t, j + 1);
+                    }
+                }
+                if (!ok) break;
                 mma_commit(&sh.vempty[s]);
-                mma_commit(&sh.pvdone);
+                if (next) mma_commit(&sh.kempty[(j + 1) & 1]);
             }
             mma_commit(&sh.mmadone);
             wait_bar(sh, p.status, &sh.mmadone, 0, false, kDrainNs);
         }
     } else if (warp >= 4) {
-        // ---------------------------------------------------------------- softmax rows
-        const int quarter = warp & 3;              // TMEM lanes 32 quarter .. + 31
-        const int r = quarter * 32 + lane;         // query row of the tile
-        const int qrow = qi * BQ + r;              // token position
-        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        float m = -INFINITY, l = 0.0f;
-        bool ok = true;
-        for (int j = 0; j < nkv; ++j) {
-            const int s = j & 1;
-            const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
-            if (!__all_sync(0xffffffffu, wait_bar(sh, p.status, &sh.sfull[s], ph))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t sa = tm + TM_S + s * BKV + lane_off;
-            uint32_t xu[BKV];
-#pragma unroll
-            for (int c = 0; c < BKV / 32; ++c) LA_TMEM_LD32(sa + c * 32, (xu + c * 32));
-            tmem_wait_ld();
-            // keys after the query or past N are masked; a tile below the diagonal and
-            // inside N (the same for every row of the tile) needs no mask
-            const int k0 = j * BKV;
-            if (!(j < qi && k0 + BKV <= p.N)) {
-                const int kmax = min(qrow, p.N - 1) - k0;  // last allowed key of this tile
-#pragma unroll
-                for (int c = 0; c < BKV; ++c)
-                    if (c > kmax) xu[c] = __float_as_uint(-INFINITY);
-            }
-            // the row max on raw scores (the scale is positive), four chains
-            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int c = 0; c < BKV; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], __uint_as_float(xu[c]));
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-            const float m_new = fmaxf(m, mx * p.scale_log2);   // base-2 units
-            const float m_use = m_new == -INFINITY ? 0.0f : m_new;  // a row with no key yet
-            const float alpha = ex2_approx(m - m_use);
-            float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            uint32_t pk[BKV / 2];
-#pragma unroll
-            for (int c = 0; c < BKV / 2; ++c) {
-                const float p0 = ex2_approx(fmaf(__uint_as_float(xu[2 * c]), p.scale_log2, -m_use));
-                const float p1 =
-                    ex2_approx(fmaf(__uint_as_float(xu[2 * c + 1]), p.scale_log2, -m_use));
-                sum4[c & 3] += p0 + p1;
-                pk[c] = pack_bf16x2(p0, p1);
-            }
-            l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
-            m = m_new;
-            LA_TMEM_ST32(sa, pk);
-            LA_TMEM_ST32(sa + 32, (pk + 32));
-            tmem_wait_st();
-            if (j > 0) {
-                // O holds PV_{j-1} once it is done; rescale rows whose max moved
-                if (!__all_sync(0xffffffffu,
-                                wait_bar(sh, p.status, &sh.pvdone,
-                                         static_cast<uint32_t>(j - 1) & 1u))) {
+        // ------------------------------------------------------------ softmax rows
+        const int t = (warp - 4) >> 2;              // query tile of this warpgroup
+        const int quarter = warp & 3;               // TMEM lanes 32 quarter .. + 31
+        if (t < ntile) {
+            const int qi = q0 + t;
+            const int nkv_t = qi + 1;
+            const int r = quarter * 32 + lane;      // query row of the tile
+            const int qrow = qi * BQ + r;           // token position
+            const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+            const uint32_t sa = tm + TM_S + t * BKV + lane_off;
+            const uint32_t oa = tm + TM_O + t * BKV + lane_off;
+            float m = -INFINITY, l = 0.0f;
+            bool ok = true;
+            for (int j = 0; j < nkv_t; ++j) {
+                if (!__all_sync(0xffffffffu, wait_bar(sh, p.status, &sh.sfull[t],
+                                                      static_cast<uint32_t>(j) & 1u))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-                    const uint32_t oa = tm + TM_O + lane_off;
+                uint32_t xu[BKV];
+#pragma unroll
+                for (int c = 0; c < BKV / 32; ++c) LA_TMEM_LD32(sa + c * 32, (xu + c * 32));
+                tmem_wait_ld();
+                // keys after the query or past N are masked; a tile below the diagonal
+                // and inside N (the same for every row of the tile) needs no mask
+                const int k0 = j * BKV;
+                if (!(j < qi && k0 + BKV <= p.N)) {
+                    const int kmax = min(qrow, p.N - 1) - k0;  // last allowed key here
+#pragma unroll
+                    for (int c = 0; c < BKV; ++c)
+                        if (c > kmax) xu[c] = __float_as_uint(-INFINITY);
+                }
+                // the row max on raw scores (the scale is positive), four chains
+                float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int c = 0; c < BKV; ++c)
+                    mx4[c & 3] = fmaxf(mx4[c & 3], __uint_as_float(xu[c]));
+                const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+                // The reference max moves only when the row's max grows by more than
+                // kMaxSlack (base 2): probabilities stay below 2^kMaxSlack, and O and l
+                // need no rescale (and the softmax no wait on O) in most key tiles.
+                const float m_row = mx * p.scale_log2;                  // base-2 units
+                const bool move = m_row > m + kMaxSlack;
+                float alpha = 1.0f;
+                if (move) {
+                    alpha = ex2_approx(m - m_row);  // 0 for the first key tile (m = -inf)
+                    m = m_row;
+                }
+                const bool rescale = __any_sync(0xffffffffu, move) && j > 0;
+                const float m_use = m == -INFINITY ? 0.0f : m;          // no key yet
+                float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int c = 0; c < BKV / 32; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float p0 = ex2_approx(
+                            fmaf(__uint_as_float(xu[c * 32 + 2 * e]), p.scale_log2, -m_use));
+                        const float p1 = ex2_approx(
+                            fmaf(__uint_as_float(xu[c * 32 + 2 * e + 1]), p.scale_log2, -m_use));
+                        sum4[e & 3] += p0 + p1;
+                        pk[e] = pack_bf16x2(p0, p1);
+                    }
+                    LA_TMEM_ST16(sa + c * 16, pk);  // P over the first 64 columns
+                }
+                l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+                tmem_wait_st();
+                if (rescale) {
+                    // O holds the products up to key tile j - 1 once the last is done;
+                    // rescale the rows whose reference max moved (alpha = 1 elsewhere)
+                    if (!__all_sync(0xffffffffu,
+                                    wait_bar(sh, p.status, &sh.pvdone[t],
+                                             static_cast<uint32_t>(j - 1) & 1u))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t u[32];
@@ -360,34 +397,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tmem_wait_st();
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.pfull[t]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.pfull[s]);
-        }
-        // ------------------------------------------------------------ epilogue
-        if (ok && __all_sync(0xffffffffu, wait_bar(sh, p.status, &sh.pvdone,
-                                                    static_cast<uint32_t>(nkv - 1) & 1u))) {
-            tc_fence_after();
-            const float inv = 1.0f / l;
-            const uint32_t oa = tm + TM_O + lane_off;
-            __nv_bfloat16* dst =
-                p.out + ((static_cast<int64_t>(b) * p.N + qrow) * p.H + h) * D;
+            // -------------------------------------------------------- epilogue
+            if (ok && __all_sync(0xffffffffu,
+                                 wait_bar(sh, p.status, &sh.pvdone[t],
+                                          static_cast<uint32_t>(nkv_t - 1) & 1u))) {
+                tc_fence_after();
+                const float inv = 1.0f / l;
+                __nv_bfloat16* dst =
+                    p.out + ((static_cast<int64_t>(b) * p.N + qrow) * p.H + h) * D;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t u[32];
-                LA_TMEM_LD32(oa + c * 32, u);
-                tmem_wait_ld();
-                uint32_t pk[16];
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t u[32];
+                    LA_TMEM_LD32(oa + c * 32, u);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = pack_bf16x2(__uint_as_float(u[2 * e]) * inv,
-                                        __uint_as_float(u[2 * e + 1]) * inv);
-                if (qrow < p.N) {
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack_bf16x2(__uint_as_float(u[2 * e]) * inv,
+                                            __uint_as_float(u[2 * e + 1]) * inv);
+                    if (qrow < p.N) {
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                        for (int e = 0; e < 4; ++e)
+                            d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2],
+                                               pk[4 * e + 3]);
+                    }
                 }
             }
         }
@@ -509,8 +547,10 @@ extern "C" int la_softmax_attention(const void* q, const void* k, const void* v,
     prm.H = H;
     prm.N = static_cast<int>(N);
     prm.Qt = static_cast<int>(Qt);
+    prm.Qp = static_cast<int>((Qt + 1) / 2);
     prm.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(D)));
-    k_attn_fwd<<<static_cast<unsigned>(Qt * B * H), kThreads, SMEM_DYN, st>>>(mq, mk, mv, prm);
+    k_attn_fwd<<<static_cast<unsigned>(static_cast<int64_t>(prm.Qp) * B * H), kThreads, SMEM_DYN,
+                 st>>>(mq, mk, mv, prm);
     if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
     note_launches(3);
     return LA_OK;
