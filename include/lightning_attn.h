@@ -217,8 +217,10 @@ int la_qkvg_projection(const void* x, const void* w, void* q, void* k, void* v, 
  *   out      out [B][N][H][d] bf16; must not overlap q, k or v
  *   rope_base    > 1 (1e7 for MiniMax-Text-01)
  * d must be 128 (LA_ERR_UNSUPPORTED otherwise), N <= 2^30; N = 0 does nothing.  The
- * rotated copies of q and k and the cos/sin table live in the library's per-device
- * workspace (grown on demand; 2 * B*N*H*d*2 + N*256 bytes).  Scores, the softmax and
+ * rotated copies of q and k live in the library's per-device workspace (grown on
+ * demand; 2 * B*N*H*d*2 bytes).  The cos/sin table (N*256 bytes) is cached per device
+ * and rebuilt when a call needs more tokens or another base; that call waits for the
+ * rebuild on its stream, so make it before any stream capture.  Scores, the softmax and
  * P*V run in fp32 with bf16 MMA operands; each output is rounded once to bf16.  Device
  * pointers, 16-byte aligned, owned by the caller.  Argument errors are returned before
  * any launch; a bounded device wait that gives up records LA_ERR_TIMEOUT.

@@ -12,8 +12,9 @@
 //
 // Design:
 //  * k_rope_table writes cos/sin of every (token, pair) angle in fp32, each computed
-//    in fp64 (angles reach 1e6 rad at 1M tokens).  k_rope rotates q and k into
-//    library-owned copies (one RNE rounding to bf16).
+//    in fp64 (angles reach 1e6 rad at 1M tokens); the table is cached per device.
+//    k_rope rotates q and k into library-owned copies (one RNE rounding to bf16),
+//    eight threads per row with 16-byte accesses.
 //  * k_attn_fwd: one CTA per (pair of 128-query tiles, head, sequence), head-major,
 //    the pairs with the most key tiles first.  Warp 0 lane 0 loads both query tiles
 //    once and the key/value tiles of the causal range into two stages by TMA (128B
@@ -141,24 +142,41 @@ __global__ void k_rope_table(float2* __restrict__ cs, int N, double base) {
     cs[idx] = make_float2(static_cast<float>(c), static_cast<float>(s));
 }
 
-// One warp per (token, head) row of q (blockIdx.y = 0) or k (1); rows are [B][N][H]:
-// lane l rotates the pair (l, l + 32) by the row's token angle and copies features
-// 64 + l and 96 + l.
+// Eight threads per (token, head) row of q (blockIdx.y = 0) or k (1); rows are
+// [B][N][H].  Thread c < 4 rotates the pairs (8c + e, 8c + e + 32), e < 8, by the row's
+// token angles; thread c >= 4 copies features [64 + 16(c - 4), + 16).  16-byte accesses.
 __global__ void k_rope(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                        __nv_bfloat16* __restrict__ qr, __nv_bfloat16* __restrict__ kr,
                        const float2* __restrict__ cs, int64_t rows, int H, int N) {
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+    const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 3;
     if (row >= rows) return;
-    const int lane = threadIdx.x & 31;
-    const __nv_bfloat16* src = (blockIdx.y == 0 ? q : k) + row * D;
-    __nv_bfloat16* dst = (blockIdx.y == 0 ? qr : kr) + row * D;
+    const int c = threadIdx.x & 7;
+    const uint4* src = reinterpret_cast<const uint4*>((blockIdx.y == 0 ? q : k) + row * D);
+    uint4* dst = reinterpret_cast<uint4*>((blockIdx.y == 0 ? qr : kr) + row * D);
+    if (c >= 4) {
+        const int o = 8 + 2 * (c - 4);  // 16-byte chunk index of feature 64 + 16(c - 4)
+        dst[o] = src[o];
+        dst[o + 1] = src[o + 1];
+        return;
+    }
     const int64_t t = (row / H) % N;  // token position within its sequence
-    const float2 r = cs[t * kPairs + lane];
-    const float a = __bfloat162float(src[lane]), b = __bfloat162float(src[lane + 32]);
-    dst[lane] = __float2bfloat16_rn(a * r.x - b * r.y);
-    dst[lane + 32] = __float2bfloat16_rn(a * r.y + b * r.x);
-    dst[64 + lane] = src[64 + lane];
-    dst[96 + lane] = src[96 + lane];
+    const uint4 a4 = src[c], b4 = src[c + 4];
+    const uint32_t* a = reinterpret_cast<const uint32_t*>(&a4);
+    const uint32_t* b = reinterpret_cast<const uint32_t*>(&b4);
+    const float4* cs4 = reinterpret_cast<const float4*>(cs + t * kPairs + 8 * c);
+    uint4 ra4, rb4;
+    uint32_t* ra = reinterpret_cast<uint32_t*>(&ra4);
+    uint32_t* rb = reinterpret_cast<uint32_t*>(&rb4);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float4 r = cs4[e];  // (cos, sin) of pairs 8c + 2e and 8c + 2e + 1
+        const float a0 = __uint_as_float(a[e] << 16), a1 = __uint_as_float(a[e] & 0xFFFF0000u);
+        const float b0 = __uint_as_float(b[e] << 16), b1 = __uint_as_float(b[e] & 0xFFFF0000u);
+        ra[e] = pack_bf16x2(a0 * r.x - b0 * r.y, a1 * r.z - b1 * r.w);
+        rb[e] = pack_bf16x2(a0 * r.y + b0 * r.x, a1 * r.w + b1 * r.z);
+    }
+    dst[c] = ra4;
+    dst[c + 4] = rb4;
 }
 
 // ------------------------------------------------------------------ attention
@@ -487,6 +505,51 @@ bool prepare_device() {
     return true;
 }
 
+// The cos/sin table of the current device for at least N tokens and this base, built
+// on `st` when it grows or the base changes (the host then waits for it once, so calls
+// on other streams find it complete).
+struct RopeTable {
+    float2* cs = nullptr;
+    int64_t n = 0;
+    double base = 0.0;
+};
+RopeTable g_tables[64];
+std::mutex g_table_mutex;
+
+int rope_table(int64_t N, double base, cudaStream_t st, const float2** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return LA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_table_mutex);
+    RopeTable& tb = g_tables[dev];
+    if (tb.cs && tb.n >= N && tb.base == base) {
+        *out = tb.cs;
+        return LA_OK;
+    }
+    const int64_t n = N > tb.n ? N : tb.n;
+    if (n > tb.n) {
+        if (tb.cs) cudaFree(tb.cs);  // waits for work already queued on the device
+        tb.cs = nullptr;
+        tb.n = 0;
+        if (cudaMalloc(&tb.cs, static_cast<size_t>(n) * kPairs * sizeof(float2)) != cudaSuccess) {
+            cudaGetLastError();
+            tb.cs = nullptr;
+            return LA_ERR_NOMEM;
+        }
+    }
+    const int64_t nt = n * kPairs;
+    k_rope_table<<<static_cast<unsigned>((nt + 255) / 256), 256, 0, st>>>(tb.cs, static_cast<int>(n),
+                                                                         base);
+    if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess) {
+        tb.n = 0;
+        return LA_ERR_CUDA;
+    }
+    note_launches(1);
+    tb.n = n;
+    tb.base = base;
+    *out = tb.cs;
+    return LA_OK;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
@@ -521,19 +584,17 @@ extern "C" int la_softmax_attention(const void* q, const void* k, const void* v,
     if (N == 0) return LA_OK;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
     if (!prepare_device()) return LA_ERR_CUDA;
-    // workspace: rotated q and k (bf16), then the cos/sin table
-    const size_t table_bytes = static_cast<size_t>(N) * kPairs * sizeof(float2);
+    // workspace: rotated q and k (bf16); the cos/sin table is cached per device
     Workspace ws;
-    int rc = workspace_acquire(2 * bytes + table_bytes, st, &ws);
+    int rc = workspace_acquire(2 * bytes, st, &ws);
     if (rc != LA_OK) return rc;
     auto* qr = static_cast<__nv_bfloat16*>(ws.base);
     auto* kr = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws.base) + bytes);
-    auto* cs = reinterpret_cast<float2*>(static_cast<char*>(ws.base) + 2 * bytes);
-    const int64_t nt = N * kPairs;
-    k_rope_table<<<static_cast<unsigned>((nt + 255) / 256), 256, 0, st>>>(cs, static_cast<int>(N),
-                                                                         rope_base);
+    const float2* cs = nullptr;
+    rc = rope_table(N, rope_base, st, &cs);
+    if (rc != LA_OK) return rc;
     const int64_t rows = static_cast<int64_t>(B) * N * H;
-    k_rope<<<dim3(static_cast<unsigned>((rows + 7) / 8), 2), 256, 0, st>>>(
+    k_rope<<<dim3(static_cast<unsigned>((rows * 8 + 255) / 256), 2), 256, 0, st>>>(
         static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), qr, kr, cs,
         rows, H, static_cast<int>(N));
     CUtensorMap mq, mk, mv;
@@ -552,6 +613,6 @@ extern "C" int la_softmax_attention(const void* q, const void* k, const void* v,
     k_attn_fwd<<<static_cast<unsigned>(static_cast<int64_t>(prm.Qp) * B * H), kThreads, SMEM_DYN,
                  st>>>(mq, mk, mv, prm);
     if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
-    note_launches(3);
+    note_launches(2);
     return LA_OK;
 }
