@@ -516,6 +516,14 @@ struct RopeTable {
 RopeTable g_tables[64];
 std::mutex g_table_mutex;
 
+struct TableReaper {
+    ~TableReaper() {
+        // Process teardown: the driver may already be gone; ignore errors.
+        for (auto& t : g_tables)
+            if (t.cs) cudaFree(t.cs);
+    }
+} g_table_reaper;
+
 int rope_table(int64_t N, double base, cudaStream_t st, const float2** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return LA_ERR_CUDA;
