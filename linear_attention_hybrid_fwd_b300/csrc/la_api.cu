@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include <atomic>
 #include <mutex>
@@ -63,6 +64,15 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
+
+// Failure-detection test hook: with LA_TEST_WITHHOLD_ARRIVAL=1 in the environment, a
+// tensor-core prefill starts with one cross-CTA arrival counter off its sentinel, so
+// one chunk never gathers all its head halves.  Every wait in the kernel is bounded, so
+// the launch ends with LA_ERR_TIMEOUT in the status word and the context stays usable.
+bool withhold_requested() {
+    const char* e = getenv("LA_TEST_WITHHOLD_ARRIVAL");
+    return e && e[0] == '1';
+}
 
 }  // namespace
 
@@ -268,6 +278,13 @@ int la_prefill_ex(const void* q, const void* k, const void* v, const void* g, vo
         const int items = prefill_tc_items(B, N);
         rc = xch_acquire(prefill_tc_flag_words(items), prefill_tc_part_floats(items, H), st, &xl);
         if (rc != LA_OK) return rc;
+        if (withhold_requested()) {
+            // failure-detection test: chunk 0's arrival counter starts off its sentinel,
+            // as if one head half's arrival were lost; the launch's waits run out
+            // (bounded) and the status word reads LA_ERR_TIMEOUT
+            if (cudaMemsetAsync(xl.use, 0, sizeof(unsigned), st) != cudaSuccess)
+                return LA_ERR_CUDA;
+        }
         return launch_prefill_tc(q, k, v, g, out, kv_state_in, kv_state_out, y_debug, B, H, N,
                                  eps, (flags & LA_FLAG_ACTIVATED) != 0, ws, xl, st);
     }
