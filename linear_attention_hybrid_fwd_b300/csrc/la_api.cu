@@ -221,7 +221,7 @@ const char* la_status_string(int s) {
     }
 }
 
-int la_version(void) { return 100; }
+int la_version(void) { return 200; }  // 0.2.0: + varlen, projection, softmax layer
 
 int64_t la_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
