@@ -16,19 +16,20 @@
 //  * The activations are not duplicated: CTA 0 loads q and applies SiLU, CTA 1 does the
 //    same for k, and each bulk-copies its activated 128 x 128 tile into the other's
 //    shared memory.  Each CTA activates its own 64 columns of v.  Both then form the
-//    full score tile Q^ K^T (two 128 x 64 halves, cheap MMAs) and their halves of the
-//    products.
+//    full 128 x 128 score tile Q^ K^T (one N = 128 MMA chain: 64 tensor cycles per k-step
+//    against 2 x 48 for two N = 64 halves on B300) and their halves of the products.
 //  * Warp roles of a head's CTA (28 warps): warp 0 issues TMA loads (lane 0: q or k and
 //    v; lane 1: g), warp 1 issues tcgen05 MMAs; warps 4-11 apply SiLU in shared memory
 //    and push the activated tile to the peer; warps 12-15 convert the fp32 state to the
 //    bf16 operand of Q^ S and mask each score half into the bf16 P operand (written in
-//    place over it); warps 16-19 post each chunk's per-token sums of squares; warps
+//    place over it; a key block wholly below a warp's rows is converted without
+//    selects); warps 16-19 post each chunk's per-token sums of squares; warps
 //    20-23 and 24-27 take alternate chunks and finish them (norm, gate, TMA store).
 //  * The RMSNorm spans all heads of a token.  The SMs the head pairs leave free run
 //    reducer CTAs in the same co-resident grid: each head half posts its 128 per-token
 //    sums of squares to a global slot and counts itself in; a reducer waits (bounded)
-//    for all 2H halves of a chunk, sums them in a fixed order (deterministic) and
-//    publishes the chunk's 128 norm factors, whose slots hold an "empty" bit pattern
+//    for all 2H halves of a chunk, sums them with all its threads in a fixed order
+//    (deterministic) and publishes the chunk's 128 norm factors, whose slots hold an "empty" bit pattern
 //    until written, so the finishing warps read their factor with one load.  A launch
 //    resets the previous launch's counters and factors in the other of two banks.  y
 //    stays in TMEM (five buffers) while the exchange is in flight.  The host checks
@@ -39,12 +40,14 @@
 //  * A batch is a list of (sequence, chunk) items run in order: B sequences of N tokens,
 //    or sequences of any lengths packed back to back (the rows of a chunk past its
 //    sequence's end are zeroed after loading, so they add nothing to any product).
-//  * SiLU(x) = x/2 (1 + tanh(x/2)) and sigmoid(x) = (1 + tanh(x/2))/2 with the hardware
-//    tanh approximation: one SFU operation per element.
+//  * SiLU(x) = x/2 (1 + tanh(x/2)) and y r sigmoid(g) = a + a tanh(g/2) (a = y r / 2) with
+//    the hardware tanh approximation: one SFU operation per element; x/2 and g/2 are
+//    taken on the packed bf16 pair (exact), which saves an instruction per element on
+//    an issue-bound path.
 //  * Every wait is bounded (%globaltimer); a CTA that gives up records LA_ERR_TIMEOUT
 //    in the status word, drains its in-flight copies and MMAs, frees TMEM and exits.
 //
-// TMEM columns: [0,64) scores half 0 (P over its first 32) | [64,128) half 1 |
+// TMEM columns: [0,128) scores, keys 0-63 then 64-127 (P of each half over its first 32) |
 //               [128,192) S (fp32, this CTA's 64 columns) | [192,512) Y0 .. Y4.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -84,7 +87,7 @@ constexpr uint32_t TM_A = 0, TM_S = 128, TM_Y = 192;
 constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s
 constexpr uint64_t kDrainNs = 200000000ull;     // 0.2 s
 
-constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 64, 0, 0);   // A K-major, B K-major
+constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 128, 0, 0);  // A K-major, B K-major
 constexpr uint32_t IDESC_QS = idesc_bf16_f32(128, DV, 0, 1);   // A K-major, B MN-major
 constexpr uint32_t IDESC_KV = idesc_bf16_f32(128, DV, 1, 1);   // A MN-major, B MN-major
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, DV, 0, 1);   // A (TMEM), B MN-major
@@ -105,6 +108,7 @@ struct Params {
     int B, H;
     int64_t N;           // tokens per sequence (the packed token count for varlen)
     int Nc;              // chunks per sequence (uniform batches)
+    uint64_t nc_magic;   // floor((2^64 - 1) / Nc): umulhi64(it, nc_magic) is it / Nc or one less
     int total;           // iterations: (sequence, chunk) items in order
     float eps;
     float inv_width;     // 1 / (H * d)
@@ -126,7 +130,12 @@ __device__ __forceinline__ Item item_at(const Params& p, int it) {
         r.b = e.z;
         r.first = e.w;
     } else {
-        const int b = it / p.Nc, c = it - b * p.Nc;
+        int b = static_cast<int>(__umul64hi(static_cast<uint64_t>(it), p.nc_magic));
+        int c = it - b * p.Nc;
+        if (c >= p.Nc) {  // the estimate is at most one low
+            ++b;
+            c -= p.Nc;
+        }
         const int64_t rem = p.N - static_cast<int64_t>(c) * CH;
         r.y = c * CH;
         r.z = b;
@@ -147,7 +156,7 @@ struct Shared {
     int issued;      // iterations whose q or k loads the producer issued
     int xin_seen;    // iterations whose peer tile the MMA issuer consumed
     int g_issued;    // iterations whose g tile was issued
-    float red[2][CH];  // reducer: per-token sums over the heads, one row per d_v half
+    float red[kThreads / 128][CH];  // reducer: per-token sums over ranges of head halves
 };
 
 // ------------------------------------------------------------------ numerics
@@ -157,14 +166,7 @@ __device__ __forceinline__ float tanh_approx(float x) {
     return y;
 }
 // SiLU(x) = x sigmoid(x) = h (1 + tanh(h)) with h = x/2.
-__device__ __forceinline__ float silu_t(float x) {
-    const float h = 0.5f * x;
-    return fmaf(h, tanh_approx(h), h);
-}
-// sigmoid(x) = (1 + tanh(x/2)) / 2.
-__device__ __forceinline__ float sigmoid_t(float x) {
-    return fmaf(0.5f, tanh_approx(0.5f * x), 0.5f);
-}
+__device__ __forceinline__ float silu_h(float h) { return fmaf(h, tanh_approx(h), h); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
@@ -173,8 +175,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+// Both bf16 halves times 1/2 (exact: a power-of-two scaling of a bf16 value).
+__device__ __forceinline__ uint32_t half_bf16x2(uint32_t u) {
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(u), "r"(0x3F003F00u));
+    return r;
+}
 __device__ __forceinline__ uint32_t silu_bf16x2(uint32_t u) {
-    return pack_bf16x2(silu_t(bf_lo(u)), silu_t(bf_hi(u)));
+    const uint32_t hh = half_bf16x2(u);
+    return pack_bf16x2(silu_h(bf_lo(hh)), silu_h(bf_hi(hh)));
 }
 __device__ __forceinline__ uint4 silu_chunk(uint4 v) {
     return make_uint4(silu_bf16x2(v.x), silu_bf16x2(v.y), silu_bf16x2(v.z), silu_bf16x2(v.w));
@@ -281,36 +290,41 @@ __device__ bool spin_until(Shared& sh, int* status, const unsigned* cnt, unsigne
 }
 
 // Reducer CTA: for its chunks (every R-th), waits for all 2H head halves' per-token sums
-// of squares, adds them in a fixed order (per d_v half over the heads in order, then
-// the two halves) and publishes r_t = 1 / sqrt(mean + eps) for the chunk's 128 tokens.
-__device__ void reducer(Shared& sh, const Params& p, int j, int R) {
+// of squares and publishes r_t = 1 / sqrt(mean + eps) for the chunk's 128 tokens.  Its
+// kThreads / 128 groups of 128 threads (one per token) each add a fixed range of head
+// halves in order; the ranges' sums are then added in range order (deterministic).
+__device__ void reducer(Shared& sh, float (*red)[CH], const Params& p, int j, int R) {
+    constexpr int G = kThreads / CH;  // 7 groups
     const int tid = threadIdx.x;
-    if (tid >= 2 * CH) return;
-    const int t = tid & (CH - 1), r = tid >> 7;
+    const int t = tid & (CH - 1), gidx = tid >> 7;
     const bool leader = tid == 0;
-    const int H = p.H, total = p.total;
-    const unsigned target = kXchEmpty + 2u * static_cast<unsigned>(H);
+    const int H2 = 2 * p.H, total = p.total;
+    const int per = (H2 + G - 1) / G;
+    const int lo = gidx * per, hi = lo + per < H2 ? lo + per : H2;
+    const unsigned target = kXchEmpty + static_cast<unsigned>(H2);
     for (int it = j; it < total; it += R) {
         if (leader) sh.verdict[0] = spin_until(sh, p.status, p.cnt + it, target) ? 1 : 0;
-        named_bar_sync(1, 2 * CH);
+        __syncthreads();
         if (!*reinterpret_cast<volatile int*>(&sh.verdict[0])) break;
-        const float* src = p.part + (static_cast<size_t>(it) * 2 * H + r) * CH + t;
+        const float* src = p.part + static_cast<size_t>(it) * H2 * CH + t;
         float acc = 0.f;
-        for (int h0 = 0; h0 < H; h0 += 32) {
-            float v[32];
+        for (int k0 = lo; k0 < hi; k0 += 8) {
+            float v[8];
 #pragma unroll
-            for (int k = 0; k < 32; ++k)
-                v[k] = h0 + k < H ? __ldcg(src + static_cast<size_t>(2 * (h0 + k)) * CH) : 0.f;
+            for (int k = 0; k < 8; ++k)
+                v[k] = k0 + k < hi ? __ldcg(src + static_cast<size_t>(k0 + k) * CH) : 0.f;
 #pragma unroll
-            for (int k = 0; k < 32; ++k) acc += v[k];
+            for (int k = 0; k < 8; ++k) acc += v[k];
         }
-        sh.red[r][t] = acc;
-        named_bar_sync(1, 2 * CH);
-        if (r == 0) {
-            const float tot = sh.red[0][t] + sh.red[1][t];
+        red[gidx][t] = acc;
+        __syncthreads();
+        if (gidx == 0) {
+            float tot = 0.f;
+#pragma unroll
+            for (int g = 0; g < G; ++g) tot += red[g][t];
             __stcg(p.rn + static_cast<size_t>(it) * CH + t, rsqrtf(tot * p.inv_width + p.eps));
         }
-        named_bar_sync(1, 2 * CH);  // sh.red is rewritten by the next chunk
+        __syncthreads();  // red is rewritten by the next chunk
     }
 }
 
@@ -351,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             sh.verdict[0] = 0;
         }
         __syncthreads();
-        reducer(sh, p, static_cast<int>(blockIdx.x) - 2 * H, static_cast<int>(gridDim.x) - 2 * H);
+        reducer(sh, sh.red, p, static_cast<int>(blockIdx.x) - 2 * H, static_cast<int>(gridDim.x) - 2 * H);
         return;
     }
 
@@ -450,17 +464,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t va = sbase + OFF_VB + s * HALF, sb = sbase + OFF_SB;
                 const uint32_t tY = tm + TM_Y + yb * DV;
                 bool ok = true;
-                // scores, in two halves of 64 key tokens: A_j = Q^ K^_j^T (128 x 64)
-                for (int j = 0; j < 2 && ok; ++j) {
-                    if (!wait_bar(sh, p.status, &sh.aempty[j], par ^ 1u)) { ok = false; break; }
-                    tc_fence_after();
+                // scores A = Q^ K^T (128 x 128), once P V^ has read both halves of A
+                if (!wait_bar(sh, p.status, &sh.aempty[0], par ^ 1u) ||
+                    !wait_bar(sh, p.status, &sh.aempty[1], par ^ 1u))
+                    break;
+                tc_fence_after();
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_ss(tm + TM_A + 64 * j, desc_kmajor(qa, ks),
-                               desc_kmajor(ka + 8192 * j, ks), IDESC_QK, ks > 0);
-                    mma_commit(&sh.afull[j]);
-                }
-                if (!ok) break;
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_ss(tm + TM_A, desc_kmajor(qa, ks), desc_kmajor(ka, ks), IDESC_QK, ks > 0);
+                mma_commit(&sh.afull[0]);
+                mma_commit(&sh.afull[1]);
                 if (!wait_bar(sh, p.status, &sh.yempty[yb], yph ^ 1u)) break;
                 if (!wait_bar(sh, p.status, &sh.sready, par)) break;
                 tc_fence_after();
@@ -634,7 +647,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int part = 0; part < 2; ++part) {
                     const int sb0 = 64 * j + 32 * part;  // first key token of these columns
                     uint32_t pk[16];
-                    if (sb0 <= q4 * 32 + 31) {  // some lane of this warp has s <= t here
+                    if (sb0 + 31 < q4 * 32) {  // every key of these columns is <= every token
+                        uint32_t r[32];
+                        LA_TMEM_LD32(tA + 32 * part, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj)
+                            pk[jj] = pack_bf16x2(__uint_as_float(r[2 * jj]),
+                                                 __uint_as_float(r[2 * jj + 1]));
+                    } else if (sb0 <= q4 * 32 + 31) {  // the warp's diagonal block
                         uint32_t r[32];
                         LA_TMEM_LD32(tA + 32 * part, r);
                         tmem_wait_ld();
@@ -671,17 +692,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t yph = static_cast<uint32_t>(it / kYBufs) & 1u;
             if (!group_wait(sh, p.status, &sh.yfull[yb], yph, leader, 3, 128, 2)) break;
             tc_fence_after();
-            float ss = 0.f;
+            float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
                 uint32_t y[32];
                 LA_TMEM_LD32(lb + TM_Y + yb * DV + 32 * part, y);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    ss = fmaf(__uint_as_float(y[j]), __uint_as_float(y[j]), ss);
+                for (int j = 0; j < 32; j += 2) {
+                    ss0 = fmaf(__uint_as_float(y[j]), __uint_as_float(y[j]), ss0);
+                    ss1 = fmaf(__uint_as_float(y[j + 1]), __uint_as_float(y[j + 1]), ss1);
+                }
             }
-            __stcg(p.part + (static_cast<size_t>(it) * 2 * H + 2 * h + rank) * CH + t, ss);
+            __stcg(p.part + (static_cast<size_t>(it) * 2 * H + 2 * h + rank) * CH + t, ss0 + ss1);
             named_bar_sync(3, 128);
             if (leader) red_release_gpu_add(p.cnt + it, 1u);  // orders the group's stores
         }
@@ -729,6 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!group_wait(sh, p.status, &sh.yfull[yb], yph, leader, bar_id, 128, slot)) break;
             tc_fence_after();
             uint8_t* gt = sm + OFF_GB + gs * HALF;
+            const float hrn = 0.5f * rn;
             const bool valid = t < im.nvalid;
             const size_t grow =
                 (static_cast<size_t>(im.z) * p.N + static_cast<size_t>(im.y) + t) * H * D + col0;
@@ -753,10 +777,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t w[4];
 #pragma unroll
                     for (int k2 = 0; k2 < 4; ++k2) {
-                        const float y0 = __uint_as_float(y[8 * j + 2 * k2]) * rn;
-                        const float y1 = __uint_as_float(y[8 * j + 2 * k2 + 1]) * rn;
-                        w[k2] = pack_bf16x2(y0 * sigmoid_t(bf_lo(gw[k2])),
-                                            y1 * sigmoid_t(bf_hi(gw[k2])));
+                        // y r sigmoid(g) = a + a tanh(g/2) with a = y r / 2
+                        const uint32_t hg = half_bf16x2(gw[k2]);
+                        const float a0 = __uint_as_float(y[8 * j + 2 * k2]) * hrn;
+                        const float a1 = __uint_as_float(y[8 * j + 2 * k2 + 1]) * hrn;
+                        w[k2] = pack_bf16x2(fmaf(a0, tanh_approx(bf_lo(hg)), a0),
+                                            fmaf(a1, tanh_approx(bf_hi(hg)), a1));
                     }
                     *gp = make_uint4(w[0], w[1], w[2], w[3]);
                 }
@@ -957,6 +983,7 @@ int launch_items(const void* q, const void* k, const void* v, const void* g, voi
     prm.H = H;
     prm.N = N;
     prm.Nc = static_cast<int>((N + CH - 1) / CH);
+    prm.nc_magic = ~0ull / static_cast<uint64_t>(prm.Nc);
     prm.total = total;
     prm.eps = eps;
     prm.inv_width = 1.0f / static_cast<float>(H * D);
