@@ -87,7 +87,8 @@ int la_decode_step(float* kv_state, const void* q, const void* k, const void* v,
                    const void* g, void* out, int B, int H, int d);
 
 /*
- * Extended prefill.
+ * Extended prefill.  bf16 runs the tensor-core kernel (LA_ERR_UNSUPPORTED for a shape it
+ * does not cover, see la_prefill_path); LA_F32, or LA_FLAG_SIMT, the CUDA-core kernel.
  *   kv_state_in  in  [B][H][d][d] fp32 initial state, or NULL for zeros; lets a long
  *                    sequence be processed in pieces (the state is the resume point)
  *   kv_state_out out [B][H][d][d] fp32 or NULL; may equal kv_state_in
@@ -132,17 +133,24 @@ int la_prefill_varlen(const void* q, const void* k, const void* v, const void* g
                       int d);
 
 /* Extended decode step: as la_decode_step with dtype, eps, an optional fp32 pre-norm
-   y_debug [B][H][d] (or NULL) and a stream. */
+   y_debug [B][H][d] (or NULL; it must not overlap any other argument) and a stream. */
 int la_decode_step_ex(float* kv_state, const void* q, const void* k, const void* v,
                       const void* g, void* out, float* y_debug, int B, int H, int d,
                       int dtype, float eps, void* cuda_stream);
 
 /* Which prefill kernel la_prefill_ex would run for this shape on the current device:
-   0 = tensor-core kernel, 1 = CUDA-core kernel, or -(la_status) if the arguments are
-   invalid.  The tensor-core kernel covers bf16, d = 128, H smaller than the number
-   of two-CTA clusters the device holds at once (it keeps every head resident for the
-   cross-head RMSNorm, runs the B sequences one after another, and needs at least one
-   more cluster for the norm's reducers), N <= 2^30 and B * ceil(N / 128) <= 131072. */
+   0 = tensor-core kernel, 1 = CUDA-core kernel, or -(la_status) if la_prefill_ex would
+   refuse the call.  bf16 I/O runs the tensor-core kernel, and LA_F32 or LA_FLAG_SIMT
+   the CUDA-core kernel; there is no silent switch between them: bf16 without
+   LA_FLAG_SIMT on a shape the tensor-core kernel does not cover gives
+   -LA_ERR_UNSUPPORTED (and la_prefill_ex returns LA_ERR_UNSUPPORTED).  The tensor-core
+   kernel covers d = 128, H smaller than the number of two-CTA clusters the device holds
+   at once (73 on a 148-SM B300: it keeps every head resident for the cross-head RMSNorm,
+   runs the B sequences one after another, and needs at least one more cluster for the
+   norm's reducers), N <= 2^30 and B * ceil(N / 128) <= 2^23.  The kernel's cross-CTA
+   waits assume its CTAs run together: a concurrent kernel on another stream that
+   holds SMs can delay it, and one that holds them past the 4 s wait bound makes the
+   prefill record LA_ERR_TIMEOUT. */
 int la_prefill_path(int B, int H, int64_t N, int d, int dtype, unsigned flags);
 
 /*
@@ -160,6 +168,10 @@ int la_prefill_path(int B, int H, int64_t N, int d, int dtype, unsigned flags);
  *   - the first call on a device looks the array's device address up (one
  *     cudaGetSymbolAddress with that device current) and caches it; make that first
  *     call before any stream capture on that device;
+ *   - the runtime loads device code lazily by default, so that first call is also
+ *     when the array most likely takes its device memory: make it before reserving
+ *     the rest of the device's memory for a pool (or set CUDA_MODULE_LOADING=EAGER,
+ *     which places the array when the library is loaded);
  *   - all calls on a device share the one array and it keeps the last call's
  *     contents: calls whose kernels may overlap on the GPU (different streams with
  *     no ordering between them) race on it and must be ordered by the caller.

@@ -18,6 +18,7 @@ Functions carry the C names:
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -139,6 +140,8 @@ def _dtype_code(t):
 
 
 def _check(ts, names):
+    """Checks that every given tensor is a contiguous CUDA tensor on one device; returns
+    that device."""
     import torch
     dev = None
     for t, n in zip(ts, names):
@@ -152,6 +155,20 @@ def _check(ts, names):
             dev = t.device
         elif t.device != dev:
             raise ValueError(f"{n} is on {t.device}, expected {dev}")
+    return dev
+
+
+@contextlib.contextmanager
+def _on_device(dev):
+    """Makes the tensors' device current for the library call: the library launches on,
+    and keeps its workspace for, the current device, and the stream handle is taken
+    from the current device's current stream."""
+    import torch
+    if dev is None or dev.index is None or dev.index == torch.cuda.current_device():
+        yield
+    else:
+        with torch.cuda.device(dev):
+            yield
 
 
 def _prefill_flags(simt, activated):
@@ -185,10 +202,11 @@ def la_prefill(q, k, v, g, out=None, kv_state_out=None, kv_state_in=None, y_debu
             raise ValueError(f"{n} must be float32 [B, H, d, d]")
     if y_debug is not None and (y_debug.shape != q.shape or y_debug.dtype != torch.float32):
         raise ValueError("y_debug must be float32 [B, N, H, d]")
-    rc = load_library().la_prefill_ex(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out), _ptr(kv_state_out), _ptr(kv_state_in),
-        _ptr(y_debug), B, H, N, d, _dtype_code(q), float(eps), _prefill_flags(simt, activated),
-        _stream_handle(stream))
+    with _on_device(q.device):
+        rc = load_library().la_prefill_ex(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out), _ptr(kv_state_out),
+            _ptr(kv_state_in), _ptr(y_debug), B, H, N, d, _dtype_code(q), float(eps),
+            _prefill_flags(simt, activated), _stream_handle(stream))
     if rc != LA_OK:
         raise LaError(rc, "la_prefill")
     return out, kv_state_out
@@ -225,10 +243,11 @@ def la_prefill_varlen(q, k, v, g, cu_seqlens, out=None, kv_state_out=None, kv_st
     if y_debug is not None and (y_debug.shape != q.shape or y_debug.dtype != torch.float32):
         raise ValueError("y_debug must be float32 [T, H, d]")
     cu_arr = (ctypes.c_int64 * (S + 1))(*cu)
-    rc = load_library().la_prefill_varlen_ex(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out), _ptr(kv_state_out), _ptr(kv_state_in),
-        _ptr(y_debug), cu_arr, S, H, d, _dtype_code(q), float(eps), _prefill_flags(simt, activated),
-        _stream_handle(stream))
+    with _on_device(q.device):
+        rc = load_library().la_prefill_varlen_ex(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out), _ptr(kv_state_out),
+            _ptr(kv_state_in), _ptr(y_debug), cu_arr, S, H, d, _dtype_code(q), float(eps),
+            _prefill_flags(simt, activated), _stream_handle(stream))
     if rc != LA_OK:
         raise LaError(rc, "la_prefill_varlen")
     return out, kv_state_out
@@ -256,9 +275,10 @@ def la_qkvg_projection(x, w, H: int, d: int = 128, activate: bool = True, out=No
     for t in out:
         if tuple(t.shape) != (T, H, d):
             raise ValueError(f"outputs must be [{T}, {H}, {d}]")
-    rc = load_library().la_qkvg_projection(
-        _ptr(x), _ptr(w), *(_ptr(t) for t in out), T, hidden, H, d,
-        LA_PROJ_SILU if activate else 0, _stream_handle(stream))
+    with _on_device(x.device):
+        rc = load_library().la_qkvg_projection(
+            _ptr(x), _ptr(w), *(_ptr(t) for t in out), T, hidden, H, d,
+            LA_PROJ_SILU if activate else 0, _stream_handle(stream))
     if rc != LA_OK:
         raise LaError(rc, "la_qkvg_projection")
     return out
@@ -278,8 +298,9 @@ def la_softmax_attention(q, k, v, out=None, rope_base: float = 1.0e7, stream=Non
             raise ValueError(f"{n} must match q in shape and dtype")
     if q.dtype != torch.bfloat16:
         raise ValueError("la_softmax_attention takes bf16 tensors")
-    rc = load_library().la_softmax_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, N, d,
-                                             float(rope_base), _stream_handle(stream))
+    with _on_device(q.device):
+        rc = load_library().la_softmax_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H,
+                                                 N, d, float(rope_base), _stream_handle(stream))
     if rc != LA_OK:
         raise LaError(rc, "la_softmax_attention")
     return out
@@ -300,9 +321,10 @@ def la_decode_step(kv_state, q, k, v, g, out=None, y_debug=None, eps: float = 1e
             raise ValueError(f"{n} must match q in shape and dtype")
     if kv_state.shape != (B, H, d, d) or kv_state.dtype != torch.float32:
         raise ValueError("kv_state must be float32 [B, H, d, d]")
-    rc = load_library().la_decode_step_ex(
-        _ptr(kv_state), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out), _ptr(y_debug), B, H, d,
-        _dtype_code(q), float(eps), _stream_handle(stream))
+    with _on_device(q.device):
+        rc = load_library().la_decode_step_ex(
+            _ptr(kv_state), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out), _ptr(y_debug), B,
+            H, d, _dtype_code(q), float(eps), _stream_handle(stream))
     if rc != LA_OK:
         raise LaError(rc, "la_decode_step")
     return out
@@ -321,9 +343,10 @@ def la_decode_step_noalloc(kv_state, q, k, v, g, out, eps: float = 1e-6, stream=
             raise ValueError(f"{n} must match q in shape and dtype")
     if tuple(kv_state.shape) != (B, H, d, d) or kv_state.dtype != _float32():
         raise ValueError("kv_state must be float32 [B, H, d, d]")
-    rc = load_library().la_decode_step_noalloc(
-        _ptr(kv_state), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out), B, H, d,
-        _dtype_code(q), float(eps), _stream_handle(stream))
+    with _on_device(q.device):
+        rc = load_library().la_decode_step_noalloc(
+            _ptr(kv_state), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out), B, H, d,
+            _dtype_code(q), float(eps), _stream_handle(stream))
     if rc != LA_OK:
         raise LaError(rc, "la_decode_step_noalloc")
     return out

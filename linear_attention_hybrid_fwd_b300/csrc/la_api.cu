@@ -269,7 +269,10 @@ int la_prefill_ex(const void* q, const void* k, const void* v, const void* g, vo
         return LA_OK;
     }
 
-    const bool use_tc = bf16 && !(flags & LA_FLAG_SIMT) && prefill_tc_supported(B, H, N) == LA_OK;
+    // bf16 runs on the tensor-core kernel unless the caller asks for the CUDA-core one;
+    // a shape the tensor-core kernel does not cover is refused, not switched silently
+    const bool use_tc = bf16 && !(flags & LA_FLAG_SIMT);
+    if (use_tc && prefill_tc_supported(B, H, N) != LA_OK) return LA_ERR_UNSUPPORTED;
     if (use_tc) {
         Workspace ws;
         int rc = workspace_acquire(0, st, &ws);
@@ -307,9 +310,9 @@ int la_prefill_path(int B, int H, int64_t N, int d, int dtype, unsigned flags) {
     if (dtype != LA_BF16 && dtype != LA_F32) return -LA_ERR_INVALID_ARG;
     if (flags & ~(LA_FLAG_SIMT | LA_FLAG_ACTIVATED)) return -LA_ERR_INVALID_ARG;
     if (d != kHeadDim) return -LA_ERR_UNSUPPORTED;
-    const bool tc = dtype == LA_BF16 && !(flags & LA_FLAG_SIMT) && N > 0 &&
-                    prefill_tc_supported(B, H, N) == LA_OK;
-    return tc ? 0 : 1;
+    if (dtype != LA_BF16 || (flags & LA_FLAG_SIMT)) return 1;
+    if (N == 0) return 0;  // nothing is launched
+    return prefill_tc_supported(B, H, N) == LA_OK ? 0 : -LA_ERR_UNSUPPORTED;
 }
 
 int la_prefill(const void* q, const void* k, const void* v, const void* g, void* out,
@@ -370,8 +373,8 @@ int la_prefill_varlen_ex(const void* q, const void* k, const void* v, const void
     }
     if (T == 0) return LA_OK;
 
-    const bool use_tc =
-        bf16 && !(flags & LA_FLAG_SIMT) && prefill_tc_supported(1, H, T) == LA_OK;
+    const bool use_tc = bf16 && !(flags & LA_FLAG_SIMT);
+    if (use_tc && prefill_tc_supported(1, H, T) != LA_OK) return LA_ERR_UNSUPPORTED;
     if (use_tc) {
         std::vector<int4> items;
         for (int b = 0; b < num_seqs; ++b) {
@@ -444,6 +447,14 @@ int la_decode_step_ex(float* kv_state, const void* q, const void* k, const void*
         if (overlaps(kv_state, state_bytes, p, io_bytes)) return LA_ERR_INVALID_ARG;
     }
     if (overlaps(kv_state, state_bytes, out, io_bytes)) return LA_ERR_INVALID_ARG;
+    if (y_debug) {  // fp32 [B][H][d], written by the kernel
+        const size_t y_bytes = (size_t)B * H * d * sizeof(float);
+        for (const void* p : ins)
+            if (overlaps(y_debug, y_bytes, p, io_bytes)) return LA_ERR_INVALID_ARG;
+        if (overlaps(y_debug, y_bytes, out, io_bytes) ||
+            overlaps(y_debug, y_bytes, kv_state, state_bytes))
+            return LA_ERR_INVALID_ARG;
+    }
 
     const size_t ny = (size_t)B * H * d;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);

@@ -14,6 +14,12 @@
 // exits.  Host code cannot use the array's name as a device address (on the host it
 // names a host-side shadow), so the first call on each device looks the address up
 // with cudaGetSymbolAddress while that device is current and caches it.
+//
+// The CUDA runtime loads a library's device code lazily by default, so the array is
+// most likely materialised on a device by that first lookup, not when the library is
+// loaded.  A caller that reserves all free device memory for its own pool should make
+// its first call on each device before reserving the pool (or run with
+// CUDA_MODULE_LOADING=EAGER, which materialises the array when the library loads).
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>

@@ -119,6 +119,45 @@ def test_decode_rejects_on_host(lib, args, want):
     assert rc == want
 
 
+def test_decode_y_debug_must_not_overlap(lib):
+    # the kernel writes fp32 y over [B][H][d]: it may not land on an input, out or the state
+    for y in (P[0], P[1], P[4], P[6]):
+        rc = lib.la_decode_step_ex(P[0], P[1], P[2], P[3], P[4], P[6], y, 2, 2, 128,
+                                   la.LA_BF16, 1e-6, None)
+        assert rc == la.LA_ERR_INVALID_ARG
+
+
+def test_wrappers_make_the_tensors_device_current(monkeypatch):
+    # the library launches on, and keeps its workspace for, the current device; the
+    # wrappers switch to the tensors' device around the call when it is another one
+    import torch
+    calls = []
+
+    class Guard:
+        def __init__(self, dev):
+            calls.append(("switch", dev.index))
+
+        def __enter__(self):
+            return self
+
+        def __exit__(self, *exc):
+            calls.append(("back",))
+
+    class Dev:
+        def __init__(self, index):
+            self.index = index
+
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    monkeypatch.setattr(torch.cuda, "device", Guard)
+    with la._on_device(Dev(3)):
+        calls.append(("call",))
+    assert calls == [("switch", 3), ("call",), ("back",)]
+    calls.clear()
+    with la._on_device(Dev(0)):
+        calls.append(("call",))
+    assert calls == [("call",)]
+
+
 def test_prefill_path_rejects_on_host(lib):
     assert lib.la_prefill_path(0, 1, 1, 128, la.LA_BF16, 0) == -la.LA_ERR_INVALID_ARG
     assert lib.la_prefill_path(1, 1, 1, 64, la.LA_BF16, 0) == -la.LA_ERR_UNSUPPORTED

@@ -31,7 +31,21 @@ def _inputs(torch, B, N, H, dtype, scale, seed):
     return make_prefill_inputs(B, N, H, 128, dtype, scale, seed, "cuda")
 
 
-def _check_prefill(env, B, N, H, dt, scale, seed, simt, S0=False):
+def _check_head_rows(y, ref_y, yabs, lim):
+    """The error of each head's d-row of y relative to that row's own maximum.  A row can
+    exceed ``lim`` only by cancellation: its reference is then small against the
+    magnitudes that make it up (max|y_ref| < 0.05 max Y_abs of the row)."""
+    num = np.abs(y - ref_y).max(-1)
+    den = np.abs(ref_y).max(-1)
+    err = num / np.where(den > 0, den, 1.0)
+    big = err > lim
+    cancel = den < 0.05 * np.abs(yabs).max(-1)
+    print(f"per-head y rows: worst {err.max():.3e}, {int(big.sum())} of {err.size} above "
+          f"{lim:g}, all of them cancellation rows: {bool(cancel[big].all())}")
+    assert cancel[big].all(), "a head row above the bound is not a cancellation row"
+
+
+def _check_prefill(env, B, N, H, dt, scale, seed, simt, S0=False, per_head=False):
     torch, la, orc = env
     dtype = torch.bfloat16 if dt == "bf16" else torch.float32
     q, k, v, g = _inputs(torch, B, N, H, dtype, scale, seed)
@@ -55,6 +69,8 @@ def _check_prefill(env, B, N, H, dt, scale, seed, simt, S0=False):
     assert e_out <= tol["out"], f"out rel err {e_out:.3e}"
     assert e_y <= tol["y_row"], f"y token-row err {e_y:.3e}"
     assert ok_elem, f"y exceeds the elementwise bound by x{worst:.2f}"
+    if per_head:
+        _check_head_rows(host64(y), ref_y, yabs, tol["y_row"])
     ok_S, msg = state_ok(orc, host64(S), ref_S, host64(k), host64(v),
                          None if S_in is None else host64(S_in), dt)
     assert ok_S, msg
@@ -93,14 +109,32 @@ def test_f32_shapes(env):
     _check_prefill(env, 2, 200, 3, "f32", 1.0, 31, simt=True, S0=True)
 
 
+def test_tensor_core_head_limit(env):
+    """The tensor-core kernel keeps every head pair and at least one reducer pair resident:
+    at the largest head count it takes (73 two-CTA clusters on a 148-SM B300) it matches
+    the oracle; one head more, bf16 without LA_FLAG_SIMT is refused (no silent switch of
+    kernel), and with LA_FLAG_SIMT the CUDA-core kernel serves it."""
+    torch, la, orc = env
+    h_max = max(h for h in range(1, 129) if la.la_prefill_path(1, h, 300) == 0)
+    assert h_max >= 64, h_max
+    assert all(la.la_prefill_path(1, h, 300) == -la.LA_ERR_UNSUPPORTED
+               for h in range(h_max + 1, h_max + 4))
+    _check_prefill(env, 1, 300, h_max, "bf16", 0.5, 17, simt=False)
+    q, k, v, g = _inputs(torch, 1, 300, h_max + 1, torch.bfloat16, 0.5, 18)
+    with pytest.raises(la.LaError) as e:
+        la.la_prefill(q, k, v, g)
+    assert e.value.status == la.LA_ERR_UNSUPPORTED
+    _check_prefill(env, 1, 300, h_max + 1, "bf16", 0.5, 18, simt=True)
+
+
 def test_prefill_8k_workload_full(env):
     """B1 H64 N8192 d128 bf16, inputs N(0,1)*0.5: every output and the final state."""
     from linear_attention_hybrid_fwd_b300.inputs import WORKLOADS
     w = WORKLOADS["prefill_8k"]
-    _check_prefill(env, w.B, w.N, w.H, "bf16", w.scale, w.seed, simt=False)
+    _check_prefill(env, w.B, w.N, w.H, "bf16", w.scale, w.seed, simt=False, per_head=True)
 
 
-def _check_long_windows(env, name, n_windows, slab=8192):
+def _check_long_windows(env, name, n_windows, slab=8192, want_y=False):
     """Long prefill: the whole sequence runs on the GPU; the oracle carries the fp64
     state through the sequence in slabs (oracle.state_pass, all heads) and runs the
     full layer on ``n_windows`` seeded 4096-token windows from the state at each
@@ -111,7 +145,9 @@ def _check_long_windows(env, name, n_windows, slab=8192):
     from linear_attention_hybrid_fwd_b300.inputs import WORKLOADS
     w = WORKLOADS[name]
     q, k, v, g = _inputs(torch, w.B, w.N, w.H, torch.bfloat16, w.scale, w.seed)
-    out, S = la.la_prefill(q, k, v, g)
+    y = (torch.empty((w.B, w.N, w.H, 128), device="cuda", dtype=torch.float32)
+         if want_y else None)
+    out, S = la.la_prefill(q, k, v, g, y_debug=y)
     torch.cuda.synchronize()
     assert la.la_get_device_status() == 0
     assert la.la_prefill_path(w.B, w.H, w.N) == 0
@@ -129,8 +165,12 @@ def _check_long_windows(env, name, n_windows, slab=8192):
         if hsel is None:
             break
         sl = slice(t0, t0 + W)
-        ref_out, _, _ = orc.prefill(host64(q[:, sl]), host64(k[:, sl]), host64(v[:, sl]),
-                                    host64(g[:, sl]), S0=S_run)
+        ref_out, ref_y, _ = orc.prefill(host64(q[:, sl]), host64(k[:, sl]),
+                                        host64(v[:, sl]), host64(g[:, sl]), S0=S_run)
+        if want_y:  # pre-norm y of the window, per token row of H*d features
+            e_y = row_rel_err(host64(y[:, sl]), ref_y, axes=(-2, -1))
+            assert e_y <= TOL["bf16"]["y_row"], f"window {t0}: y token-row err {e_y:.3e}"
+
         got = host64(out[:, sl])
         e_all = rel_max_err(got, ref_out)
         e_head = rel_max_err(got[:, :, hsel], ref_out[:, :, hsel])
@@ -143,8 +183,9 @@ def _check_long_windows(env, name, n_windows, slab=8192):
 
 
 def test_prefill_128k_workload_windows(env):
-    """B1 H64 N131072 d128 bf16: two seeded windows and the final state."""
-    _check_long_windows(env, "prefill_128k", 2)
+    """B1 H64 N131072 d128 bf16: two seeded windows (output and pre-norm y) and the final
+    state."""
+    _check_long_windows(env, "prefill_128k", 2, want_y=True)
 
 
 def test_prefill_1m_workload_windows(env):
