@@ -20,6 +20,7 @@ is needed between steps.  Printed as one JSON line:
   N8192, TFLOP/s of the causal product against the measured bf16 peak
 * ``varlen``: a packed batch of 64K tokens in sequences of seeded lengths (1..8192)
   through ``la_prefill_varlen``, tokens/s and GB/s
+* ``state_pass``: the state-only pass over the same k and v (``la_state_pass``), GB/s
 * ``e2e``: the same prefill with pinned host inputs, the H2D copies and the D2H
   copy of the output inside the timed region
 * ``cpu_baseline``: the fp64 oracle on a bounded sample, on this host's cores
@@ -56,6 +57,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-varlen", action="store_true")
     ap.add_argument("--no-projection", action="store_true")
     ap.add_argument("--no-attention", action="store_true")
+    ap.add_argument("--no-state", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -402,6 +404,8 @@ def run_ours(a):
     if not a.no_varlen:
         line["varlen"] = bench_varlen(a, torch, la, WORKLOADS["prefill_varlen_64k"], dev,
                                       stream, peaks, make_prefill_inputs, rank)
+    if not a.no_state:
+        line["state_pass"] = bench_state_pass(a, torch, la, w, dev, stream, peaks, k, v)
     if not a.no_e2e:
         line["e2e"] = bench_e2e(a, torch, la, q, k, v, g, out, S, stream, world, dev)
     del q, k, v, g, out
@@ -573,6 +577,32 @@ def bench_varlen(a, torch, la, w, dev, stream, peaks, make_prefill_inputs, rank)
             "ms_per_step": ms, "tokens_per_s": w.N / (ms / 1e3), "bytes_per_step": nbytes,
             "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
             "gpu_launches_per_step": launches / len(per)}
+
+
+def bench_state_pass(a, torch, la, w, dev, stream, peaks, k, v):
+    """The state-only pass over the headline workload's k and v (what a rank of a
+    sequence-sharded prefill computes for the ranks after it): k and v read, the fp32
+    state written, per step."""
+    S = torch.empty((w.B, w.H, w.d, w.d), device=dev, dtype=torch.float32)
+
+    def step():
+        la.la_state_pass(k, v, kv_state_out=S)
+
+    for _ in range(max(a.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if la.la_get_device_status() != 0:
+        raise SystemExit("device status error after the state-pass warm-up")
+    n0 = la.la_launch_count()
+    per = time_steps(torch, step, max(min(a.steps, 100), 10), stream)
+    launches = la.la_launch_count() - n0
+    ms = sum(per) / len(per)
+    nbytes = 2.0 * w.B * w.N * w.H * w.d * 2 + w.B * w.H * w.d * w.d * 4
+    gbs = nbytes / (ms / 1e3) / 1e9
+    del S
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "ms_per_step": ms,
+            "tokens_per_s": w.B * w.N / (ms / 1e3), "bytes_per_step": nbytes, "GB/s": gbs,
+            "frac_hbm": gbs / peaks["hbm_gbs"], "gpu_launches_per_step": launches / len(per)}
 
 
 def bench_e2e(a, torch, la, q, k, v, g, out, S, stream, world, dev):

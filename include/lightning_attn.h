@@ -184,6 +184,40 @@ int la_decode_step_noalloc(float* kv_state, const void* q, const void* k, const 
                            const void* g, void* out, int B, int H, int d, int dtype,
                            float eps, void* cuda_stream);
 
+/*
+ * State of a run of tokens without its outputs ("Hybrid Modeling", MiniMax-01 deep dive,
+ * Hugging Face blog: step 2's SiLU on K and V and step 3's K^T V, the d x d state of the
+ * O(d^2 n) route):
+ *     kv_state_out[b][h] = kv_state_in[b][h] + sum_t SiLU(k[b][t][h])^T SiLU(v[b][t][h])
+ * i.e. the state la_prefill reaches after the same N tokens, at two fifths of its memory
+ * traffic (k and v are read; q, g and out are not touched).  A rank of a
+ * sequence-sharded prefill takes the states of the ranks before it from this.
+ *   k, v          in  [B][N][H][d] bf16, pre-activation (or activated with
+ *                     LA_FLAG_ACTIVATED in flags)
+ *   kv_state_in   in  [B][H][d][d] fp32, or NULL for zeros
+ *   kv_state_out  out [B][H][d][d] fp32; may equal kv_state_in, must not overlap k or v
+ * bf16 only (LA_ERR_UNSUPPORTED for LA_F32), d = 128.  N = 0 copies (or zeroes) the
+ * state.  The tokens of each (b, h) are split into segments summed on tensor cores and
+ * the segments' fp32 states are added in a fixed order (deterministic); the segment
+ * states live in the library's per-device workspace.  Device pointers, 16-byte aligned;
+ * argument errors are returned before any launch; a bounded device wait that gives up
+ * records LA_ERR_TIMEOUT.
+ */
+int la_state_pass(const void* k, const void* v, float* kv_state_out, const float* kv_state_in,
+                  int B, int H, int64_t N, int d, int dtype, unsigned flags, void* cuda_stream);
+
+/*
+ * Fixed-order sum of fp32 arrays, for the state prefix of a sequence-sharded prefill
+ * (the state a rank continues from is the sum of the states of the ranks before it):
+ *     out[j] = (base ? base[j] : 0) + parts[0][j] + parts[1][j] + ... + parts[count-1][j]
+ * added left to right, so every rank that sums the same arrays gets the same bits.
+ *   parts  in  [count][n] fp32 (count >= 0);  base in [n] fp32 or NULL;  out out [n] fp32
+ * n a multiple of 4; out may equal base and must not overlap parts.  Device pointers,
+ * 16-byte aligned.  Argument errors are returned before any launch.
+ */
+int la_state_sum(const float* parts, int count, const float* base, float* out, int64_t n,
+                 void* cuda_stream);
+
 /* Static text for an la_status value. */
 const char* la_status_string(int status);
 

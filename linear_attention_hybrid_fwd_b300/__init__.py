@@ -13,6 +13,8 @@ Functions carry the C names:
 * ``la_decode_step(kv_state, q, ...)``  -- one token per sequence, ``[B, H, d]`` inputs
 * ``la_decode_step_noalloc``           -- the same step with the library's fixed scratch,
                                           for callers that cannot let it allocate
+* ``la_state_pass(k, v, ...)``         -- the state after a run of tokens, no outputs
+* ``la_state_sum(parts, base)``        -- fixed-order sum of states (sharded prefill)
 * ``la_prefill_path``                  -- which prefill kernel serves a shape
 * ``la_status_string``, ``la_get_device_status``, ``la_version``, ``la_launch_count``
 """
@@ -23,6 +25,7 @@ import ctypes
 import os
 
 __all__ = ["la_prefill", "la_prefill_varlen", "la_decode_step", "la_decode_step_noalloc",
+           "la_state_pass", "la_state_sum",
            "la_qkvg_projection", "la_softmax_attention", "la_status_string", "la_get_device_status", "la_version",
            "la_launch_count", "la_prefill_path", "LaError", "library_path", "load_library",
            "LA_BF16", "LA_F32", "LA_FLAG_SIMT", "LA_FLAG_ACTIVATED", "LA_PROJ_SILU"]
@@ -91,6 +94,10 @@ def load_library():
     lib.la_softmax_attention.argtypes = [vp, vp, vp, vp, i32, i32, i64, i32, ctypes.c_double,
                                          vp]
     lib.la_softmax_attention.restype = i32
+    lib.la_state_pass.argtypes = [vp, vp, fp, fp, i32, i32, i64, i32, i32, u32, vp]
+    lib.la_state_pass.restype = i32
+    lib.la_state_sum.argtypes = [fp, i32, fp, fp, i64, vp]
+    lib.la_state_sum.restype = i32
     lib.la_launch_count.argtypes = []
     lib.la_launch_count.restype = ctypes.c_int64
     _lib = lib
@@ -349,6 +356,52 @@ def la_decode_step_noalloc(kv_state, q, k, v, g, out, eps: float = 1e-6, stream=
             _dtype_code(q), float(eps), _stream_handle(stream))
     if rc != LA_OK:
         raise LaError(rc, "la_decode_step_noalloc")
+    return out
+
+
+def la_state_pass(k, v, kv_state_out=None, kv_state_in=None, activated: bool = False,
+                  stream=None):
+    """State after the tokens of ``k, v`` (bf16 ``[B, N, H, d]``) without computing
+    outputs: ``kv_state_in + SiLU(K)^T SiLU(V)`` per (sequence, head), fp32
+    ``[B, H, d, d]``.  ``activated``: k and v are already SiLU-activated."""
+    import torch
+    B, N, H, d = k.shape
+    if kv_state_out is None:
+        kv_state_out = torch.empty((B, H, d, d), device=k.device, dtype=torch.float32)
+    _check([k, v, kv_state_out, kv_state_in], ["k", "v", "kv_state_out", "kv_state_in"])
+    if v.shape != k.shape or v.dtype != k.dtype:
+        raise ValueError("v must match k in shape and dtype")
+    for t, n in ((kv_state_out, "kv_state_out"), (kv_state_in, "kv_state_in")):
+        if t is not None and (tuple(t.shape) != (B, H, d, d) or t.dtype != torch.float32):
+            raise ValueError(f"{n} must be float32 [B, H, d, d]")
+    with _on_device(k.device):
+        rc = load_library().la_state_pass(
+            _ptr(k), _ptr(v), _ptr(kv_state_out), _ptr(kv_state_in), B, H, N, d,
+            _dtype_code(k), LA_FLAG_ACTIVATED if activated else 0, _stream_handle(stream))
+    if rc != LA_OK:
+        raise LaError(rc, "la_state_pass")
+    return kv_state_out
+
+
+def la_state_sum(parts, base=None, out=None, stream=None):
+    """``base + parts[0] + ... + parts[-1]`` added in that order (fp32 arrays; ``parts``
+    is ``[count, ...]``, ``base`` and ``out`` shaped like ``parts[0]``)."""
+    import torch
+    shape = tuple(parts.shape[1:])
+    if out is None:
+        out = torch.empty(shape, device=parts.device, dtype=torch.float32)
+    _check([parts, base, out], ["parts", "base", "out"])
+    for t, n in ((parts, "parts"), (base, "base"), (out, "out")):
+        if t is not None and t.dtype != torch.float32:
+            raise ValueError(f"{n} must be float32")
+    for t, n in ((base, "base"), (out, "out")):
+        if t is not None and tuple(t.shape) != shape:
+            raise ValueError(f"{n} must have the shape of parts[0]")
+    with _on_device(parts.device):
+        rc = load_library().la_state_sum(_ptr(parts), int(parts.shape[0]), _ptr(base),
+                                         _ptr(out), out.numel(), _stream_handle(stream))
+    if rc != LA_OK:
+        raise LaError(rc, "la_state_sum")
     return out
 
 

@@ -472,6 +472,62 @@ int la_decode_step(float* kv_state, const void* q, const void* k, const void* v,
                              nullptr);
 }
 
+int la_state_pass(const void* k, const void* v, float* kv_state_out, const float* kv_state_in,
+                  int B, int H, int64_t N, int d, int dtype, unsigned flags, void* cuda_stream) {
+    // ---- host-side validation: nothing is launched or written on failure ----
+    if (B <= 0 || H <= 0 || N < 0 || d <= 0 || !kv_state_out) return LA_ERR_INVALID_ARG;
+    if (dtype != LA_BF16 && dtype != LA_F32) return LA_ERR_INVALID_ARG;
+    if (flags & ~LA_FLAG_ACTIVATED) return LA_ERR_INVALID_ARG;
+    if (d != kHeadDim || dtype != LA_BF16) return LA_ERR_UNSUPPORTED;
+    if (B > 65535 || H > 65535) return LA_ERR_UNSUPPORTED;
+    if (N > (int64_t(1) << 40) / ((int64_t)B * H * d)) return LA_ERR_INVALID_ARG;
+    if (N > 0 && (!k || !v)) return LA_ERR_INVALID_ARG;
+    const void* ptrs[] = {k, v, kv_state_out, kv_state_in};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return LA_ERR_MISALIGNED;
+    const size_t io_bytes = (size_t)B * N * H * d * 2;
+    const size_t state_bytes = (size_t)B * H * d * d * sizeof(float);
+    if (N > 0 && (overlaps(kv_state_out, state_bytes, k, io_bytes) ||
+                  overlaps(kv_state_out, state_bytes, v, io_bytes)))
+        return LA_ERR_INVALID_ARG;
+    if (kv_state_in && kv_state_in != kv_state_out &&
+        overlaps(kv_state_in, state_bytes, kv_state_out, state_bytes))
+        return LA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
+    const int64_t n = (int64_t)B * H * d * d;
+    if (N == 0) {
+        if (kv_state_in == kv_state_out) return LA_OK;
+        if (kv_state_in)
+            return cuda_status(cudaMemcpyAsync(kv_state_out, kv_state_in, state_bytes,
+                                               cudaMemcpyDeviceToDevice, st));
+        return launch_zero_state(kv_state_out, n, st);
+    }
+    const int nseg = state_segments(B, H, N);
+    Workspace ws;
+    int rc = workspace_acquire((size_t)nseg * state_bytes, st, &ws);
+    if (rc != LA_OK) return rc;
+    float* part = static_cast<float*>(ws.base);
+    rc = launch_state_tc(k, v, part, B, H, N, nseg, (flags & LA_FLAG_ACTIVATED) != 0, ws.status,
+                         st);
+    if (rc != LA_OK) return rc;
+    return launch_sum_rows(part, nseg, n, kv_state_in, kv_state_out, st);
+}
+
+int la_state_sum(const float* parts, int count, const float* base, float* out, int64_t n,
+                 void* cuda_stream) {
+    if (count < 0 || n < 0 || !out || (n % 4) != 0) return LA_ERR_INVALID_ARG;
+    if (count > 0 && !parts) return LA_ERR_INVALID_ARG;
+    const void* ptrs[] = {parts, base, out};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return LA_ERR_MISALIGNED;
+    const size_t bytes = (size_t)n * sizeof(float);
+    if (count > 0 && overlaps(out, bytes, parts, (size_t)count * bytes)) return LA_ERR_INVALID_ARG;
+    if (base && base != out && overlaps(base, bytes, out, bytes)) return LA_ERR_INVALID_ARG;
+    if (n == 0) return LA_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
+    return launch_sum_rows(parts, count, n, base, out, st);
+}
+
 int la_get_device_status(void* cuda_stream) {
     cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
     if (cudaStreamSynchronize(st) != cudaSuccess) return LA_ERR_CUDA;

@@ -2,6 +2,7 @@
 // Not installed; the public surface is include/lightning_attn.h.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -89,5 +90,19 @@ int launch_prefill_tc_varlen(const void* q, const void* k, const void* v, const 
                              cudaStream_t st);
 // Chunk length of the tensor-core prefill (the items' granularity).
 constexpr int kTcChunk = 128;
+// The [B][N][H*d] bf16 tensor map of the tensor-core kernels (64-feature x 128-token
+// boxes, 128B swizzle); false if the driver's encoder is unavailable or refuses.
+bool encode_io_map_bf16(CUtensorMap* m, const void* base, int B, int H, int64_t N);
+
+// ---- state-only pass (la_state_tc.cu) ------------------------------------------------
+// Segments per (b, h) for a state pass over N tokens (whole 128-token chunks each).
+int state_segments(int B, int H, int64_t N);
+// Partial states part[nseg][B][H][d][d] of the segments (bf16 k, v; activated: already
+// SiLU-activated).
+int launch_state_tc(const void* k, const void* v, float* part, int B, int H, int64_t N,
+                    int nseg, bool activated, int* status, cudaStream_t st);
+// out[j] = (base ? base[j] : 0) + sum_{i < count} parts[i * n + j] in the order of i.
+int launch_sum_rows(const float* parts, int count, int64_t n, const float* base, float* out,
+                    cudaStream_t st);
 
 }  // namespace la

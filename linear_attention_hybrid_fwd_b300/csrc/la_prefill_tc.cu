@@ -932,6 +932,10 @@ int reducers_for(int H) {
 
 }  // namespace
 
+bool encode_io_map_bf16(CUtensorMap* m, const void* base, int B, int H, int64_t N) {
+    return encode_io_map(m, base, B, H, N);
+}
+
 int prefill_tc_supported(int B, int H, int64_t N) {
     if (N <= 0 || N > (int64_t(1) << 30)) return LA_ERR_UNSUPPORTED;
     const int64_t Nc = (N + CH - 1) / CH;

@@ -1,8 +1,9 @@
 """Sequence-sharded prefill (linear_attention_hybrid_fwd_b300.sharded) on CPU, gloo.
 
 Each rank holds one contiguous segment of the same sequences (uneven lengths); the
-per-rank prefill is the fp64 oracle standing in for the GPU kernel, so what is checked
-is the exchange: the state prefix each rank continues from.  The concatenated outputs
+per-rank operations (prefill, state-only pass, ordered state sum) are fp64 oracle
+stand-ins for the GPU kernels, so what is checked is the exchange: the all-gather of
+segment states and the prefix each rank continues from.  The concatenated outputs
 must equal the oracle run on the whole sequence, and the last rank's state the whole
 sequence's final state, both to fp64 rounding.
 """
@@ -38,17 +39,30 @@ def _worker(rank, world, port, q_out):
     from linear_attention_hybrid_fwd_b300.sharded import sharded_prefill
     dist.init_process_group("gloo", rank=rank, world_size=world)
 
-    def op(q, k, v, g, kv_state_in=None, eps=1e-6):
+    from oracle.state_pass import state_pass
+
+    def prefill(q, k, v, g, kv_state_in=None, eps=1e-6):
         out, _, S = oracle.prefill(q.numpy(), k.numpy(), v.numpy(), g.numpy(),
                                    S0=None if kv_state_in is None else kv_state_in.numpy(),
                                    eps=eps)
         return torch.from_numpy(out), torch.from_numpy(S)
 
+    def state(k, v):
+        return torch.from_numpy(state_pass(k, v))
+
+    def state_sum(parts, base=None):
+        acc = torch.zeros_like(parts[0]) if base is None else base.clone()
+        for p in parts:  # in rank order, as the library adds them
+            acc = acc + p
+        return acc
+
+    ops = {"prefill": prefill, "state_pass": state, "state_sum": state_sum}
+
     seg = SEGMENTS[world]
     lo = sum(seg[:rank])
     q, k, v, g = (torch.from_numpy(np.ascontiguousarray(t[:, lo:lo + seg[rank]]))
                   for t in _inputs(sum(seg)))
-    out, S = sharded_prefill(q, k, v, g, op=op)
+    out, S = sharded_prefill(q, k, v, g, ops=ops)
     q_out.put((rank, out.numpy(), S.numpy()))
     dist.barrier()
     dist.destroy_process_group()
