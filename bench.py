@@ -21,11 +21,13 @@ is needed between steps.  Printed as one JSON line:
 * ``varlen``: a packed batch of 64K tokens in sequences of seeded lengths (1..8192)
   through ``la_prefill_varlen``, tokens/s and GB/s
 * ``state_pass``: the state-only pass over the same k and v (``la_state_pass``), GB/s
+* ``prefill_128k``: the long prefill (B1 H64 N131072), GB/s against the HBM peak
 * ``e2e``: the same prefill with pinned host inputs, the H2D copies and the D2H
   copy of the output inside the timed region
 * ``cpu_baseline``: the fp64 oracle on a bounded sample, on this host's cores
 
-``--impl reference`` times the oracle instead (the reference arm).
+``--impl reference`` times the oracle instead (the reference arm); ``--oracle-table``
+times the oracle on every workload config on this host's cores.
 """
 from __future__ import annotations
 
@@ -58,6 +60,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-projection", action="store_true")
     ap.add_argument("--no-attention", action="store_true")
     ap.add_argument("--no-state", action="store_true")
+    ap.add_argument("--no-long", action="store_true", help="skip the 128K-token prefill leg")
+    ap.add_argument("--oracle-table", action="store_true",
+                    help="time the fp64 oracle on every workload config (host cores) and exit")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -270,6 +275,95 @@ def oracle_sample(w, seconds: float, seed_offset: int = 0):
     return w.B * n / t, n, used, t
 
 
+def _decode_slice(args):
+    """One process's share of the oracle decode loop (spawned worker)."""
+    import numpy as np
+    import oracle
+    S, steps, seed = args
+    rng = np.random.default_rng(seed)
+    B, H, d = S.shape[0], S.shape[1], S.shape[2]
+    ins = [tuple(rng.standard_normal((B, H, d)) * 0.5 for _ in range(4)) for _ in range(4)]
+    for t in range(steps):
+        _, _, S = oracle.decode_step(S, *ins[t % 4])
+    return S.shape
+
+
+def oracle_table(a):
+    """Host wall time of the fp64 oracle, as it stands, on every workload config: one
+    thread and all of this host's cores.  Inputs are seeded normal draws with the
+    configs' shapes and spreads (one 8192-token slab reused for the long sequences: the
+    oracle's time does not depend on the values).  Prints one JSON line."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    import numpy as np
+    import oracle
+    from oracle.state_pass import state_pass
+    oracle.build()
+    ncpu = os.cpu_count() or 1
+    rng = np.random.default_rng(0)
+    rows = []
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
+
+    def add(cfg, what, threads, secs, tokens):
+        rows.append({"config": cfg, "what": what, "threads": threads, "seconds": secs,
+                     "tokens_per_s": tokens / secs if secs > 0 else None})
+        print(json.dumps(rows[-1]), file=sys.stderr, flush=True)
+
+    # 1: tiny fp32 prefill, B1 H1 N512, N(0,1)
+    q, k, v, g = (rng.standard_normal((1, 512, 1, 128)) for _ in range(4))
+    for th in (1, ncpu):
+        add(1, "prefill B1 H1 N512", th, timed(lambda: oracle.prefill(q, k, v, g, nthreads=th)),
+            512)
+    # 2: prefill B1 H64 N8192, N(0,1) * 0.5
+    q, k, v, g = (rng.standard_normal((1, 8192, 64, 128)) * 0.5 for _ in range(4))
+    for th in (1, ncpu):
+        add(2, "prefill B1 H64 N8192", th,
+            timed(lambda: oracle.prefill(q, k, v, g, nthreads=th)), 8192)
+
+    # 3: prefill B1 H64 N131072 on all cores, in 8192-token slabs carrying the state
+    def long_prefill(slabs):
+        S = None
+        for _ in range(slabs):
+            _, _, S = oracle.prefill(q, k, v, g, S0=S, nthreads=ncpu)
+    add(3, "prefill B1 H64 N131072 (16 slabs of 8192)", ncpu, timed(lambda: long_prefill(16)),
+        131072)
+    # 4: 64 decode steps, B256 H64, from a state; the oracle's decode step is one thread,
+    # all cores by splitting the batch over spawned processes
+    S0 = rng.standard_normal((256, 64, 128, 128)) * 0.1
+    add(4, "64 decode steps B256 H64", 1, timed(lambda: _decode_slice((S0, 64, 1))), 256 * 64)
+    parts = np.array_split(S0, ncpu)
+    with cf.ProcessPoolExecutor(ncpu, mp_context=mp.get_context("spawn")) as ex:
+        list(ex.map(_decode_slice, [(p[:1], 1, 1) for p in parts]))  # start the workers
+        add(4, "64 decode steps B256 H64", ncpu,
+            timed(lambda: list(ex.map(_decode_slice, [(p, 64, i) for i, p in enumerate(parts)]))),
+            256 * 64)
+    del S0, parts
+    # 5: N = 1048576: the streaming fp64 state pass over every head (128 slabs of 8192
+    # tokens, torch fp64 on all cores) and the 8 windows of 4096 tokens, all heads, from
+    # the state at each window's start
+    import torch
+    torch.set_num_threads(ncpu)
+    kt, vt = torch.from_numpy(k), torch.from_numpy(v)
+
+    def stream_pass():
+        S = None
+        for _ in range(128):
+            S = state_pass(kt, vt, S)
+    add(5, "state pass N1048576 (128 slabs of 8192), all heads", ncpu, timed(stream_pass),
+        1048576)
+    qw, kw, vw, gw = (x[:, :4096] for x in (q, k, v, g))
+    S_start = rng.standard_normal((1, 64, 128, 128))
+    add(5, "8 windows of 4096 tokens, all heads", ncpu,
+        timed(lambda: [oracle.prefill(qw, kw, vw, gw, S0=S_start, nthreads=ncpu)
+                       for _ in range(8)]), 8 * 4096)
+    print(json.dumps({"oracle_table": rows, "host_cores": ncpu}), flush=True)
+    return 0
+
+
 def run_reference(a):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -406,6 +500,9 @@ def run_ours(a):
                                       stream, peaks, make_prefill_inputs, rank)
     if not a.no_state:
         line["state_pass"] = bench_state_pass(a, torch, la, w, dev, stream, peaks, k, v)
+    if not a.no_long and w.name == "prefill_8k":
+        line["prefill_128k"] = bench_long(a, torch, la, WORKLOADS["prefill_128k"], dev, stream,
+                                          peaks, make_prefill_inputs, rank)
     if not a.no_e2e:
         line["e2e"] = bench_e2e(a, torch, la, q, k, v, g, out, S, stream, world, dev)
     del q, k, v, g, out
@@ -579,6 +676,39 @@ def bench_varlen(a, torch, la, w, dev, stream, peaks, make_prefill_inputs, rank)
             "gpu_launches_per_step": launches / len(per)}
 
 
+def bench_long(a, torch, la, w, dev, stream, peaks, make_prefill_inputs, rank):
+    """The long prefill (B1 H64 N131072): one la_prefill per step, 10.7 GB of
+    algorithmic bytes (q, k, v, g read, out written, the state)."""
+    q, k, v, g = make_prefill_inputs(w.B, w.N, w.H, w.d, torch.bfloat16, w.scale,
+                                     w.seed + 100 * rank, dev)
+    out = torch.empty_like(q)
+    S = torch.empty((w.B, w.H, w.d, w.d), device=dev, dtype=torch.float32)
+
+    def step():
+        la.la_prefill(q, k, v, g, out=out, kv_state_out=S)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    if la.la_get_device_status() != 0:
+        raise SystemExit("device status error after the long-prefill warm-up")
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    per = time_steps(torch, step, max(min(a.steps, 10), 3), stream)
+    clk = clocks.stop()
+    ms = sum(per) / len(per)
+    nbytes = 5.0 * w.B * w.N * w.H * w.d * 2 + w.B * w.H * w.d * w.d * 4
+    gbs = nbytes / (ms / 1e3) / 1e9
+    del q, k, v, g, out, S
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "ms_per_step": ms,
+            "tokens_per_s": w.B * w.N / (ms / 1e3), "bytes_per_step": nbytes, "GB/s": gbs,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                         "kernel": "la_prefill_tc"},
+            "tflops_alg": 4.0 * w.B * w.H * w.N * w.d * w.d / (ms / 1e3) / 1e12,
+            "clocks": clk}
+
+
 def bench_state_pass(a, torch, la, w, dev, stream, peaks, k, v):
     """The state-only pass over the headline workload's k and v (what a rank of a
     sequence-sharded prefill computes for the ranks after it): k and v read, the fp32
@@ -666,6 +796,8 @@ def bench_e2e(a, torch, la, q, k, v, g, out, S, stream, world, dev):
 
 def main(argv=None):
     a = parse_args(argv)
+    if a.oracle_table:
+        return oracle_table(a)
     if a.impl == "reference":
         return run_reference(a)
     return run_ours(a)
