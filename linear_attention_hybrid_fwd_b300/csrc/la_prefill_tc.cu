@@ -24,7 +24,8 @@
 //    bf16 operand of Q^ S and mask each score half into the bf16 P operand (written in
 //    place over it; a key block wholly below a warp's rows is converted without
 //    selects); warps 16-19 post each chunk's per-token sums of squares; warps
-//    20-23 and 24-27 take alternate chunks and finish them (norm, gate, TMA store).
+//    20-23 and 24-27 finish every chunk together, each group half of y's columns
+//    (norm, gate, TMA store).
 //  * The RMSNorm spans all heads of a token.  The SMs the head pairs leave free run
 //    reducer CTAs in the same co-resident grid: each head half posts its 128 per-token
 //    sums of squares to a global slot and counts itself in; a reducer waits (bounded)
@@ -383,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int y = 0; y < kYBufs; ++y) {
             mbar_init(&sh.yfull[y], 1);
-            mbar_init(&sh.yempty[y], 1);
+            mbar_init(&sh.yempty[y], 2);  // both finishing groups
         }
         for (int i = 0; i < kGBufs; ++i) {
             mbar_init(&sh.gfull[i], 1);
@@ -709,15 +710,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader) red_release_gpu_add(p.cnt + it, 1u);  // orders the group's stores
         }
     } else if (warp >= 20) {
-        // ------------------------------------------------ finish: norm, gate, store
-        const int fg = (warp - 20) >> 2;  // 0 or 1: even or odd iterations
+        // ------------------------------------------------ finish: norm, gate, store.  Both
+        // groups take every iteration, group fg the columns [32 fg, 32 fg + 32) of y, so a
+        // y tile is read (and its TMEM freed) in half the time one group would take.
+        const int fg = (warp - 20) >> 2;
         const int q4 = warp & 3;
         const int t = q4 * 32 + lane;     // token row
         const bool leader = t == 0;
+        const bool leader2 = leader && fg == 0;  // of both groups
         const uint32_t bar_id = 4 + fg;
         const int slot = 3 + fg;
         const uint32_t lb = tm + (static_cast<uint32_t>(q4 * 32) << 16);
-        for (int it = fg; it < total; it += 2) {
+        for (int it = 0; it < total; ++it) {
             const Item im = item_at<kVarlen>(p, it);
             const int yb = it % kYBufs;
             const uint32_t yph = static_cast<uint32_t>(it / kYBufs) & 1u;
@@ -755,67 +759,65 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float hrn = 0.5f * rn;
             const bool valid = t < im.nvalid;
             const size_t grow =
-                (static_cast<size_t>(im.z) * p.N + static_cast<size_t>(im.y) + t) * H * D + col0;
+                (static_cast<size_t>(im.z) * p.N + static_cast<size_t>(im.y) + t) * H * D + col0 +
+                32 * fg;
+            uint32_t y[32];
+            LA_TMEM_LD32(lb + TM_Y + yb * DV + 32 * fg, y);
+            tmem_wait_ld();
+            tc_fence_before();
+            named_bar_sync(bar_id, 128);
+            if (leader) mbar_arrive(&sh.yempty[yb]);  // this group's half of y is read
+            if (p.y_dbg && valid) {
+                float4* yp = reinterpret_cast<float4*>(p.y_dbg + grow);
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                uint32_t y[32];
-                LA_TMEM_LD32(lb + TM_Y + yb * DV + 32 * part, y);
-                tmem_wait_ld();
-                if (p.y_dbg && valid) {
-                    float4* yp = reinterpret_cast<float4*>(p.y_dbg + grow + 32 * part);
+                for (int j = 0; j < 8; ++j)
+                    yp[j] = make_float4(__uint_as_float(y[4 * j]), __uint_as_float(y[4 * j + 1]),
+                                        __uint_as_float(y[4 * j + 2]), __uint_as_float(y[4 * j + 3]));
+            }
+            uint4 gv[4];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        yp[j] = make_float4(__uint_as_float(y[4 * j]), __uint_as_float(y[4 * j + 1]),
-                                            __uint_as_float(y[4 * j + 2]),
-                                            __uint_as_float(y[4 * j + 3]));
-                }
+            for (int j = 0; j < 4; ++j)
+                gv[j] = *reinterpret_cast<const uint4*>(gt + swz(t, 4 * fg + j));
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint4* gp = reinterpret_cast<uint4*>(gt + swz(t, 4 * part + j));
-                    const uint4 gv = *gp;
-                    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-                    uint32_t w[4];
+            for (int j = 0; j < 4; ++j) {
+                uint32_t* gw = reinterpret_cast<uint32_t*>(&gv[j]);
 #pragma unroll
-                    for (int k2 = 0; k2 < 4; ++k2) {
-                        // y r sigmoid(g) = a + a tanh(g/2) with a = y r / 2
-                        const uint32_t hg = half_bf16x2(gw[k2]);
-                        const float a0 = __uint_as_float(y[8 * j + 2 * k2]) * hrn;
-                        const float a1 = __uint_as_float(y[8 * j + 2 * k2 + 1]) * hrn;
-                        w[k2] = pack_bf16x2(fmaf(a0, tanh_approx(bf_lo(hg)), a0),
-                                            fmaf(a1, tanh_approx(bf_hi(hg)), a1));
-                    }
-                    *gp = make_uint4(w[0], w[1], w[2], w[3]);
+                for (int k2 = 0; k2 < 4; ++k2) {
+                    // y r sigmoid(g) = a + a tanh(g/2) with a = y r / 2
+                    const uint32_t hg = half_bf16x2(gw[k2]);
+                    const float a0 = __uint_as_float(y[8 * j + 2 * k2]) * hrn;
+                    const float a1 = __uint_as_float(y[8 * j + 2 * k2 + 1]) * hrn;
+                    gw[k2] = pack_bf16x2(fmaf(a0, tanh_approx(bf_lo(hg)), a0),
+                                         fmaf(a1, tanh_approx(bf_hi(hg)), a1));
                 }
             }
-            tc_fence_before();
             if (kVarlen && im.nvalid < CH) {
                 // a partial chunk of a packed batch: its last rows are the next sequence's,
-                // so only this sequence's rows are stored, row by row
-                named_bar_sync(bar_id, 128);
+                // so only this sequence's rows are stored, each thread its half row from
+                // registers.  The g tile is not written: a generic store to it could land
+                // after the next TMA load into the same buffer.
                 if (valid) {
                     uint4* orow = reinterpret_cast<uint4*>(p.out + grow);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        orow[j] = *reinterpret_cast<const uint4*>(gt + swz(t, j));
+                    for (int j = 0; j < 4; ++j) orow[j] = gv[j];
                 }
-                named_bar_sync(bar_id, 128);
-                if (leader) {
-                    mbar_arrive(&sh.yempty[yb]);
-                    mbar_arrive(&sh.gempty[gs]);
-                }
+                named_bar_sync(6, 256);  // both groups have read the g tile
+                if (leader2) mbar_arrive(&sh.gempty[gs]);
                 continue;
             }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint4*>(gt + swz(t, 4 * fg + j)) = gv[j];
             fence_proxy_async_smem();
-            named_bar_sync(bar_id, 128);
-            if (leader) {
-                mbar_arrive(&sh.yempty[yb]);
+            named_bar_sync(6, 256);  // both halves of the tile are written
+            if (leader2) {
                 tma_store_3d(&to, gt, col0, im.y, im.z);  // rows past N are dropped
                 bulk_commit_group();
                 bulk_wait_group_read0();  // the tile may take the next g once read
                 mbar_arrive(&sh.gempty[gs]);
             }
         }
-        if (leader) bulk_wait_group0();
+        if (leader2) bulk_wait_group0();
     }
 
     // ---------------------------------------------------- teardown
