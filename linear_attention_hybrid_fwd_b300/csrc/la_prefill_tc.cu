@@ -215,13 +215,15 @@ __device__ __forceinline__ void raise_abort(Shared& sh, int* status) {
 }
 // Waits for the phase of `bar` with `parity` to complete.  Gives up (false) when the
 // CTA is aborting (honor_abort) or after `limit_ns`, raising the abort itself.
-template <bool kCluster = false>
-__device__ bool wait_bar(Shared& sh, int* status, uint64_t* bar, uint32_t parity,
-                         bool honor_abort = true, uint64_t limit_ns = kTimeoutNs) {
+// The spinning part of wait_bar, out of line: a wait that succeeds at once costs no
+// instruction-cache lines at its call site.
+template <bool kCluster>
+__device__ __noinline__ bool wait_bar_spin(Shared& sh, int* status, uint64_t* bar,
+                                           uint32_t parity, bool honor_abort,
+                                           uint64_t limit_ns) {
     auto probe = [&]() {
         return kCluster ? mbar_try_wait_acq_cluster(bar, parity) : mbar_try_wait(bar, parity);
     };
-    if (probe()) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (probe()) return true;
@@ -233,6 +235,17 @@ __device__ bool wait_bar(Shared& sh, int* status, uint64_t* bar, uint32_t parity
             }
         }
     }
+}
+// Waits for the phase of `bar` with `parity` to complete.  Gives up (false) when the
+// CTA is aborting (honor_abort) or after `limit_ns`, raising the abort itself.
+template <bool kCluster = false>
+__device__ __forceinline__ bool wait_bar(Shared& sh, int* status, uint64_t* bar,
+                                         uint32_t parity, bool honor_abort = true,
+                                         uint64_t limit_ns = kTimeoutNs) {
+    const bool done =
+        kCluster ? mbar_try_wait_acq_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    if (done) return true;
+    return wait_bar_spin<kCluster>(sh, status, bar, parity, honor_abort, limit_ns);
 }
 // Group-uniform wait: thread `leader` waits (bounded), the group of `n` threads syncs on
 // named barrier `id`, then every thread observes the completed phase itself.  No
@@ -528,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (kAct && live) {
                 // already activated: nothing to do
             } else if (live) {
-#pragma unroll
+#pragma unroll 1
                 for (int g4 = 0; g4 < 2; ++g4) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
