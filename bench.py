@@ -61,6 +61,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-attention", action="store_true")
     ap.add_argument("--no-state", action="store_true")
     ap.add_argument("--no-long", action="store_true", help="skip the 128K-token prefill leg")
+    ap.add_argument("--no-segments", action="store_true",
+                    help="skip the few-heads long-sequence leg (segment-parallel vs serial)")
     ap.add_argument("--oracle-table", action="store_true",
                     help="time the fp64 oracle on every workload config (host cores) and exit")
     ap.add_argument("--no-e2e", action="store_true")
@@ -503,6 +505,9 @@ def run_ours(a):
     if not a.no_long and w.name == "prefill_8k":
         line["prefill_128k"] = bench_long(a, torch, la, WORKLOADS["prefill_128k"], dev, stream,
                                           peaks, make_prefill_inputs, rank)
+    if not a.no_segments and w.name == "prefill_8k":
+        line["segments"] = bench_segments(a, torch, la, WORKLOADS["prefill_h8_256k"], dev,
+                                          stream, peaks, make_prefill_inputs, rank)
     if not a.no_e2e:
         line["e2e"] = bench_e2e(a, torch, la, q, k, v, g, out, S, stream, world, dev)
     del q, k, v, g, out
@@ -707,6 +712,41 @@ def bench_long(a, torch, la, w, dev, stream, peaks, make_prefill_inputs, rank):
                          "kernel": "la_prefill_tc"},
             "tflops_alg": 4.0 * w.B * w.H * w.N * w.d * w.d / (ms / 1e3) / 1e12,
             "clocks": clk}
+
+
+def bench_segments(a, torch, la, w, dev, stream, peaks, make_prefill_inputs, rank):
+    """One long sequence with few heads (B1 H8 N262144): la_prefill in its
+    segment-parallel mode (state pass over the prefix segments, ordered prefix sums,
+    then all segments side by side) against the serial chunk chain (LA_FLAG_SERIAL) on
+    the same inputs.  Algorithmic bytes as for any prefill: q, k, v, g read, out
+    written, the state."""
+    q, k, v, g = make_prefill_inputs(w.B, w.N, w.H, w.d, torch.bfloat16, w.scale,
+                                     w.seed + 100 * rank, dev)
+    out = torch.empty_like(q)
+    S = torch.empty((w.B, w.H, w.d, w.d), device=dev, dtype=torch.float32)
+    nbytes = 5.0 * w.B * w.N * w.H * w.d * 2 + w.B * w.H * w.d * w.d * 4
+    res = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+           "path": la.la_prefill_path(w.B, w.H, w.N), "bytes_per_step": nbytes}
+    for name, serial in (("segmented", False), ("serial", True)):
+        def step():
+            la.la_prefill(q, k, v, g, out=out, kv_state_out=S, serial=serial)
+
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        if la.la_get_device_status() != 0:
+            raise SystemExit("device status error after the segment-leg warm-up")
+        n0 = la.la_launch_count()
+        per = time_steps(torch, step, max(min(a.steps, 20), 5), stream)
+        launches = la.la_launch_count() - n0
+        ms = sum(per) / len(per)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        res[name] = {"ms_per_step": ms, "tokens_per_s": w.B * w.N / (ms / 1e3), "GB/s": gbs,
+                     "frac_hbm": gbs / peaks["hbm_gbs"],
+                     "gpu_launches_per_step": launches / len(per)}
+    res["speedup"] = res["serial"]["ms_per_step"] / res["segmented"]["ms_per_step"]
+    del q, k, v, g, out, S
+    return res
 
 
 def bench_state_pass(a, torch, la, w, dev, stream, peaks, k, v):

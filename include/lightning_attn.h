@@ -22,7 +22,8 @@
  * Ownership and memory: every pointer is a DEVICE pointer owned by the caller
  * (16-byte aligned).  Inputs are read only and are not modified; out must not alias
  * an input.  The library owns one internal per-device workspace (exchange buffers,
- * status word), grown on demand under a mutex and freed at unload.
+ * status word), grown on demand under a mutex and freed at unload.  The prefill's
+ * exchange holds 1 MiB at H = 64 for any length plus 2 x 516 bytes per 128-token chunk.
  *
  * Execution: calls enqueue kernels on the given CUDA stream (NULL = legacy default
  * stream) and return without synchronising.  Calls on one device share the
@@ -63,6 +64,8 @@ typedef enum {
 #define LA_FLAG_ACTIVATED 2u /* prefill: q, k, v are already SiLU-activated (as
                                 la_qkvg_projection writes them with LA_PROJ_SILU);
                                 the kernels skip step 2.  g is raw either way. */
+#define LA_FLAG_SERIAL 4u /* prefill: keep one chunk chain per head even where the
+                             segment-parallel mode would run (see la_prefill_path) */
 
 /*
  * Prefill of B sequences of N tokens ("Hybrid Modeling", mechanism steps 2-4).
@@ -139,8 +142,18 @@ int la_decode_step_ex(float* kv_state, const void* q, const void* k, const void*
                       int dtype, float eps, void* cuda_stream);
 
 /* Which prefill kernel la_prefill_ex would run for this shape on the current device:
-   0 = tensor-core kernel, 1 = CUDA-core kernel, or -(la_status) if la_prefill_ex would
-   refuse the call.  bf16 I/O runs the tensor-core kernel, and LA_F32 or LA_FLAG_SIMT
+   0 = tensor-core kernel, 1 = CUDA-core kernel, 2 = tensor-core kernel in the
+   segment-parallel mode, or -(la_status) if la_prefill_ex would refuse the call.
+   The segment-parallel mode is the blockwise route's prefix over the d x d states
+   ("Hybrid Modeling": the O(d^2 n) form) spread over the SMs that a few heads leave
+   idle.  It runs for one sequence (B == 1) when the device holds at least twice H
+   head pairs plus a reducer pair and N spans at least 2 x 8192 tokens, unless
+   LA_FLAG_SERIAL is set: the tokens are cut into segments of whole 128-token chunks,
+   the state-only pass (as la_state_pass) sums K^T V^ over the tokens before each
+   segment, the per-segment states are added in a fixed order, and then every segment
+   runs its own head pairs from its prefix state, all segments in one launch.  It reads
+   k and v once more for all but the last segment.  The result is deterministic and
+   differs from the serial chain only in the order of fp32 additions of the state.  bf16 I/O runs the tensor-core kernel, and LA_F32 or LA_FLAG_SIMT
    the CUDA-core kernel; there is no silent switch between them: bf16 without
    LA_FLAG_SIMT on a shape the tensor-core kernel does not cover gives
    -LA_ERR_UNSUPPORTED (and la_prefill_ex returns LA_ERR_UNSUPPORTED).  The tensor-core

@@ -28,7 +28,8 @@ __all__ = ["la_prefill", "la_prefill_varlen", "la_decode_step", "la_decode_step_
            "la_state_pass", "la_state_sum",
            "la_qkvg_projection", "la_softmax_attention", "la_status_string", "la_get_device_status", "la_version",
            "la_launch_count", "la_prefill_path", "LaError", "library_path", "load_library",
-           "LA_BF16", "LA_F32", "LA_FLAG_SIMT", "LA_FLAG_ACTIVATED", "LA_PROJ_SILU"]
+           "LA_BF16", "LA_F32", "LA_FLAG_SIMT", "LA_FLAG_ACTIVATED", "LA_FLAG_SERIAL",
+           "LA_PROJ_SILU"]
 
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_MISALIGNED = 0, 1, 2, 3
 LA_ERR_CUDA, LA_ERR_NOMEM, LA_ERR_TIMEOUT, LA_ERR_SCRATCH_LIMIT = 4, 5, 6, 7
@@ -36,6 +37,7 @@ LA_NOALLOC_MAX_HEADS = 16384
 LA_BF16, LA_F32 = 0, 1
 LA_FLAG_SIMT = 1
 LA_FLAG_ACTIVATED = 2
+LA_FLAG_SERIAL = 4
 LA_PROJ_SILU = 1
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -113,9 +115,10 @@ def la_version() -> int:
 
 
 def la_prefill_path(B: int, H: int, N: int, d: int = 128, dtype: int = LA_BF16,
-                    simt: bool = False) -> int:
-    """0 if the tensor-core prefill kernel serves this shape, 1 for the CUDA-core one."""
-    return load_library().la_prefill_path(B, H, N, d, dtype, LA_FLAG_SIMT if simt else 0)
+                    simt: bool = False, serial: bool = False) -> int:
+    """0 if the tensor-core prefill kernel serves this shape, 1 for the CUDA-core one,
+    2 for the tensor-core kernel in the segment-parallel mode."""
+    return load_library().la_prefill_path(B, H, N, d, dtype, _prefill_flags(simt, False, serial))
 
 
 def la_launch_count() -> int:
@@ -178,20 +181,22 @@ def _on_device(dev):
             yield
 
 
-def _prefill_flags(simt, activated):
-    return (LA_FLAG_SIMT if simt else 0) | (LA_FLAG_ACTIVATED if activated else 0)
+def _prefill_flags(simt, activated, serial=False):
+    return ((LA_FLAG_SIMT if simt else 0) | (LA_FLAG_ACTIVATED if activated else 0)
+            | (LA_FLAG_SERIAL if serial else 0))
 
 
 def la_prefill(q, k, v, g, out=None, kv_state_out=None, kv_state_in=None, y_debug=None,
                eps: float = 1e-6, simt: bool = False, want_state: bool = True, stream=None,
-               activated: bool = False):
+               activated: bool = False, serial: bool = False):
     """Prefill. ``q, k, v, g``: ``[B, N, H, d]`` (bf16 or fp32, contiguous, CUDA).
 
     Returns ``(out, kv_state_out)``; ``kv_state_out`` is ``[B, H, d, d]`` fp32 (``None``
     when ``want_state`` is False and none was passed).  ``kv_state_in`` continues a
     sequence from a previous state; ``y_debug`` (fp32 ``[B, N, H, d]``) receives the
     pre-norm output.  ``simt`` selects the CUDA-core kernel.  ``activated``: q, k, v
-    are already SiLU-activated (``la_qkvg_projection(..., activate=True)``).
+    are already SiLU-activated (``la_qkvg_projection(..., activate=True)``).  ``serial``
+    keeps one chunk chain per head where the segment-parallel mode would run.
     """
     import torch
     B, N, H, d = q.shape
@@ -213,7 +218,7 @@ def la_prefill(q, k, v, g, out=None, kv_state_out=None, kv_state_in=None, y_debu
         rc = load_library().la_prefill_ex(
             _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(out), _ptr(kv_state_out),
             _ptr(kv_state_in), _ptr(y_debug), B, H, N, d, _dtype_code(q), float(eps),
-            _prefill_flags(simt, activated), _stream_handle(stream))
+            _prefill_flags(simt, activated, serial), _stream_handle(stream))
     if rc != LA_OK:
         raise LaError(rc, "la_prefill")
     return out, kv_state_out

@@ -232,7 +232,7 @@ int la_prefill_ex(const void* q, const void* k, const void* v, const void* g, vo
     if (B <= 0 || H <= 0 || N < 0 || d <= 0) return LA_ERR_INVALID_ARG;
     if (dtype != LA_BF16 && dtype != LA_F32) return LA_ERR_INVALID_ARG;
     if (!(eps >= 0.0f) || !isfinite(eps)) return LA_ERR_INVALID_ARG;
-    if (flags & ~(LA_FLAG_SIMT | LA_FLAG_ACTIVATED)) return LA_ERR_INVALID_ARG;
+    if (flags & ~(LA_FLAG_SIMT | LA_FLAG_ACTIVATED | LA_FLAG_SERIAL)) return LA_ERR_INVALID_ARG;
     if (d != kHeadDim) return LA_ERR_UNSUPPORTED;
     if (B > 65535 || H > 4096) return LA_ERR_UNSUPPORTED;
     // element counts: B*N*H*d must stay well inside int64 (the kernels index in int64)
@@ -274,12 +274,18 @@ int la_prefill_ex(const void* q, const void* k, const void* v, const void* g, vo
     const bool use_tc = bf16 && !(flags & LA_FLAG_SIMT);
     if (use_tc && prefill_tc_supported(B, H, N) != LA_OK) return LA_ERR_UNSUPPORTED;
     if (use_tc) {
+        // one long sequence with few heads: segments run side by side from prefix states
+        int seg_items = 0, fine = 1;
+        const int nseg = (flags & LA_FLAG_SERIAL) ? 1
+                                                  : prefill_tc_segment_plan(B, H, N, &seg_items, &fine);
+        const size_t set_floats = (size_t)H * d * d;  // one state per head (B == 1)
+        const size_t seg_floats = nseg > 1 ? ((size_t)(nseg - 1) * fine + nseg) * set_floats : 0;
         Workspace ws;
-        int rc = workspace_acquire(0, st, &ws);
+        int rc = workspace_acquire(seg_floats * sizeof(float), st, &ws);
         if (rc != LA_OK) return rc;
         XchLease xl;
         const int items = prefill_tc_items(B, N);
-        rc = xch_acquire(prefill_tc_flag_words(items), prefill_tc_part_floats(items, H), st, &xl);
+        rc = xch_acquire(prefill_tc_flag_words(items), prefill_tc_part_floats(H, nseg), st, &xl);
         if (rc != LA_OK) return rc;
         if (withhold_requested()) {
             // failure-detection test: chunk 0's arrival counter starts off its sentinel,
@@ -288,8 +294,23 @@ int la_prefill_ex(const void* q, const void* k, const void* v, const void* g, vo
             if (cudaMemsetAsync(xl.use, 0, sizeof(unsigned), st) != cudaSuccess)
                 return LA_ERR_CUDA;
         }
+        const bool act = (flags & LA_FLAG_ACTIVATED) != 0;
+        const float* S_seg = nullptr;
+        if (nseg > 1) {
+            // the state of the tokens before each segment: K^T V^ of fixed pieces (the
+            // state pass), then prefix[s] = S_in + the pieces before segment s, in order
+            float* pieces = static_cast<float*>(ws.base);
+            float* prefix = pieces + (size_t)(nseg - 1) * fine * set_floats;
+            const int64_t Np = (int64_t)(nseg - 1) * seg_items * 128;
+            rc = launch_state_tc(k, v, pieces, 1, H, Np, (nseg - 1) * fine, act, ws.status, st);
+            for (int s = 0; s < nseg && rc == LA_OK; ++s)
+                rc = launch_sum_rows(pieces, s * fine, (int64_t)set_floats, kv_state_in,
+                                     prefix + (size_t)s * set_floats, st);
+            if (rc != LA_OK) return rc;
+            S_seg = prefix;
+        }
         return launch_prefill_tc(q, k, v, g, out, kv_state_in, kv_state_out, y_debug, B, H, N,
-                                 eps, (flags & LA_FLAG_ACTIVATED) != 0, ws, xl, st);
+                                 eps, act, ws, xl, st, nseg, seg_items, S_seg);
     }
     // CUDA-core kernel: y in fp32 (into y_debug when given), then the norm/gate pass.
     float* y = y_debug;
@@ -308,11 +329,15 @@ int la_prefill_ex(const void* q, const void* k, const void* v, const void* g, vo
 int la_prefill_path(int B, int H, int64_t N, int d, int dtype, unsigned flags) {
     if (B <= 0 || H <= 0 || N < 0 || d <= 0) return -LA_ERR_INVALID_ARG;
     if (dtype != LA_BF16 && dtype != LA_F32) return -LA_ERR_INVALID_ARG;
-    if (flags & ~(LA_FLAG_SIMT | LA_FLAG_ACTIVATED)) return -LA_ERR_INVALID_ARG;
+    if (flags & ~(LA_FLAG_SIMT | LA_FLAG_ACTIVATED | LA_FLAG_SERIAL)) return -LA_ERR_INVALID_ARG;
     if (d != kHeadDim) return -LA_ERR_UNSUPPORTED;
     if (dtype != LA_BF16 || (flags & LA_FLAG_SIMT)) return 1;
     if (N == 0) return 0;  // nothing is launched
-    return prefill_tc_supported(B, H, N) == LA_OK ? 0 : -LA_ERR_UNSUPPORTED;
+    if (prefill_tc_supported(B, H, N) != LA_OK) return -LA_ERR_UNSUPPORTED;
+    int seg_items = 0, fine = 1;
+    if (!(flags & LA_FLAG_SERIAL) && prefill_tc_segment_plan(B, H, N, &seg_items, &fine) > 1)
+        return 2;
+    return 0;
 }
 
 int la_prefill(const void* q, const void* k, const void* v, const void* g, void* out,
@@ -329,7 +354,9 @@ int la_prefill_varlen_ex(const void* q, const void* k, const void* v, const void
     if (num_seqs <= 0 || H <= 0 || d <= 0 || !cu_seqlens) return LA_ERR_INVALID_ARG;
     if (dtype != LA_BF16 && dtype != LA_F32) return LA_ERR_INVALID_ARG;
     if (!(eps >= 0.0f) || !isfinite(eps)) return LA_ERR_INVALID_ARG;
-    if (flags & ~(LA_FLAG_SIMT | LA_FLAG_ACTIVATED)) return LA_ERR_INVALID_ARG;
+    // a packed batch always runs one chunk chain per (sequence, head): LA_FLAG_SERIAL
+    // is accepted and changes nothing
+    if (flags & ~(LA_FLAG_SIMT | LA_FLAG_ACTIVATED | LA_FLAG_SERIAL)) return LA_ERR_INVALID_ARG;
     if (d != kHeadDim) return LA_ERR_UNSUPPORTED;
     if (num_seqs > 65535 || H > 4096) return LA_ERR_UNSUPPORTED;
     if (cu_seqlens[0] != 0) return LA_ERR_INVALID_ARG;
@@ -390,7 +417,7 @@ int la_prefill_varlen_ex(const void* q, const void* k, const void* v, const void
         if (rc != LA_OK) return rc;
         const int total = static_cast<int>(items.size());
         XchLease xl;
-        rc = xch_acquire(prefill_tc_flag_words(total), prefill_tc_part_floats(total, H), st, &xl);
+        rc = xch_acquire(prefill_tc_flag_words(total), prefill_tc_part_floats(H, 1), st, &xl);
         if (rc != LA_OK) return rc;
         const int4* dev_items = nullptr;
         rc = items_upload(items, st, &dev_items);

@@ -32,9 +32,11 @@ struct Workspace {
 int workspace_acquire(size_t bytes, cudaStream_t st, Workspace* ws);
 
 // The cross-head exchange of the tensor-core prefill.  Per chunk: the per-token sums of
-// squares of every head half ("partials", written before they are read, never reset)
-// and the chunk's arrival counter and per-token norm factors ("flags"), which live in
-// two banks whose every word holds kXchEmpty until written.  A launch writes one flag
+// squares of every head half ("partials", written before they are read, never reset; a
+// ring of 16 chunks whose slot a head half reuses once the norm factors of the chunk
+// that held it are published) and the chunk's arrival counter and per-token norm
+// factors ("flags", 129 words per chunk), which live in two banks whose every word holds
+// kXchEmpty until written.  A launch writes one flag
 // bank and resets, in the other, the words that the previous launch wrote there; so
 // every flag bank is all-empty again one launch after its use and nothing runs between
 // calls.
@@ -76,11 +78,18 @@ int prefill_tc_supported(int B, int H, int64_t N);
 // (sequence, chunk) items of a batch of B sequences of N tokens
 int prefill_tc_items(int B, int64_t N);
 size_t prefill_tc_flag_words(int items);
-size_t prefill_tc_part_floats(int items, int H);
+// The partials: a ring of chunks per segment, independent of the length.
+size_t prefill_tc_part_floats(int H, int nseg);
+// Segment-parallel plan for B sequences of N tokens: the number of segments (1: the
+// serial chunk chain), their length in chunks (seg_items) and the state-pass pieces per
+// segment (fine).  Only B == 1 is cut, and only when H leaves SMs idle.
+int prefill_tc_segment_plan(int B, int H, int64_t N, int* seg_items, int* fine);
+// nseg > 1: segment s of seg_items chunks starts from S_seg[s] ([nseg][H][d][d], B == 1).
 int launch_prefill_tc(const void* q, const void* k, const void* v, const void* g, void* out,
                       const float* S_in, float* S_out, float* y_debug, int B, int H, int64_t N,
                       float eps, bool activated, const Workspace& ws, const XchLease& xl,
-                      cudaStream_t st);
+                      cudaStream_t st, int nseg = 1, int seg_items = 0,
+                      const float* S_seg = nullptr);
 // A packed batch of T tokens: items (device, `total` of them) = {first row, valid rows,
 // sequence, first chunk of its sequence}, chunks of 128 tokens in order.
 int launch_prefill_tc_varlen(const void* q, const void* k, const void* v, const void* g,

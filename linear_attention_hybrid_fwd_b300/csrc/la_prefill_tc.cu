@@ -74,6 +74,8 @@ constexpr int kThreads = 896;         // 28 warps
 constexpr int kYBufs = 5;             // y tiles in TMEM
 constexpr int kMaxReducers = 16;      // reducer CTAs (on SMs the head pairs leave free)
 constexpr int kGBufs = 2;             // g tiles in flight (TMA-loaded ahead of the epilogue)
+constexpr int kPartRing = 16;         // chunks whose per-token partials are held at once
+constexpr int kMinSegChunks = 64;     // segment mode: chunks per segment at least
 constexpr uint32_t TILE = 32768;      // 128 x 128 bf16 = two swizzled 128 x 64 halves
 constexpr uint32_t HALF = 16384;      // 128 x 64 bf16, one 128B-swizzled block
 constexpr uint32_t OFF_QB = 0;                  // 2 stages: q^ tiles
@@ -100,7 +102,8 @@ struct Params {
     float* y_dbg;
     unsigned* cnt;       // [B*Nc] head halves posted, from kXchEmpty
     float* rn;           // [B*Nc][CH] norm factors (kXchEmpty until written)
-    float* part;         // [B*Nc][2H][CH] per-token sums of squares of each head half
+    float* part;         // [kPartRing][2H][CH] per-token sums of squares of each head half,
+                         // chunk `it` in slot it % kPartRing
     uint4* xch_clear;    // the other bank's counters and factors of the previous launch
     int64_t n_clear4;    // ... as a count of 16-byte words
     int* status;
@@ -111,6 +114,9 @@ struct Params {
     int Nc;              // chunks per sequence (uniform batches)
     uint64_t nc_magic;   // floor((2^64 - 1) / Nc): umulhi64(it, nc_magic) is it / Nc or one less
     int total;           // iterations: (sequence, chunk) items in order
+    int nseg;            // segments of the item list, each run by its own head pairs (B == 1)
+    int seg_items;       // items per segment (the last may have fewer)
+    const float* S_seg;  // segment mode: [nseg][H][d][d] state before each segment
     float eps;
     float inv_width;     // 1 / (H * d)
 };
@@ -204,6 +210,19 @@ __device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int ks) {
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int ks) {
     return smem_desc_sw128(base + ks * 2048, HALF, 1024);
 }
+// A descriptor moved on by `off` bytes (a multiple of 16).  The start address is the
+// low 14-bit field (address / 16) and every operand lies below 256 KiB, so the add stays
+// in the low word.  The MMA issuer builds each stage's descriptors once per chunk and
+// moves them by constants: it issues 32 MMAs per chunk, and their issue rate, not the
+// tensor pipe, sets its pace.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t off) {
+    const uint32_t lo = static_cast<uint32_t>(d) + (off >> 4);
+    return (d & 0xFFFFFFFF00000000ull) | lo;
+}
+// Offset of k-step ks (16 elements) in a K-major 128 x 128 tile of two swizzled halves.
+__device__ __forceinline__ constexpr uint32_t kofs(int ks) {
+    return static_cast<uint32_t>((ks >> 2) * HALF + (ks & 3) * 32);
+}
 
 // ------------------------------------------------------------------ bounded waits
 __device__ __forceinline__ bool abort_set(Shared& sh) {
@@ -285,12 +304,66 @@ __device__ __forceinline__ void store_row_bf16(uint8_t* blk, int r, int part,
     }
 }
 
+// A sequence's first chunk and last chunk: the conversion warps move this CTA's 64
+// state columns of d_k row t between global memory and TMEM (out of line: once per
+// sequence, kept out of the per-chunk code).
+__device__ __noinline__ void state_rows_out(float* dst, uint32_t ts) {
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+        uint32_t r[32];
+        LA_TMEM_LD32(ts + 32 * part, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4*>(dst + 32 * part + j) =
+                make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                            __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+    }
+}
+__device__ __noinline__ void state_rows_in(const float* src, uint32_t ts, uint8_t* sbk, int t) {
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+        uint32_t r[32];
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            const float4 f = src ? *reinterpret_cast<const float4*>(src + 32 * part + j)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            r[j] = __float_as_uint(f.x);
+            r[j + 1] = __float_as_uint(f.y);
+            r[j + 2] = __float_as_uint(f.z);
+            r[j + 3] = __float_as_uint(f.w);
+        }
+        LA_TMEM_ST32(ts + 32 * part, r);
+        store_row_bf16(sbk, t, part, r);
+    }
+    tmem_wait_st();
+}
+
 // Bounded spin until *cnt == target (unsigned compare); false after a timeout (raising
 // the abort) or when the CTA is aborting.
 __device__ bool spin_until(Shared& sh, int* status, const unsigned* cnt, unsigned target) {
     uint64_t t0 = 0;
     for (;;) {
         if (ld_acquire_gpu(cnt) == target) return true;
+        if (abort_set(sh)) return false;
+        const uint64_t now = global_timer_ns();
+        if (t0 == 0) {
+            t0 = now;
+        } else if (now - t0 > kTimeoutNs) {
+            raise_abort(sh, status);
+            return false;
+        }
+        __nanosleep(200);
+    }
+}
+
+// Bounded spin until the norm factor at `slot` is published (acquire); false after a
+// timeout (raising the abort) or when the CTA is aborting.
+__device__ bool spin_published(Shared& sh, int* status, const float* slot) {
+    const unsigned* w = reinterpret_cast<const unsigned*>(slot);
+    uint64_t t0 = 0;
+    for (;;) {
+        if (ld_acquire_gpu(w) != kXchEmpty) return true;
         if (abort_set(sh)) return false;
         const uint64_t now = global_timer_ns();
         if (t0 == 0) {
@@ -316,11 +389,19 @@ __device__ void reducer(Shared& sh, float (*red)[CH], const Params& p, int j, in
     const int per = (H2 + G - 1) / G;
     const int lo = gidx * per, hi = lo + per < H2 ? lo + per : H2;
     const unsigned target = kXchEmpty + static_cast<unsigned>(H2);
-    for (int it = j; it < total; it += R) {
+    // chunks in the order the head pairs produce them: place li of every segment before
+    // place li + 1 (one segment: chunk order)
+    const int nseg = p.nseg, span = nseg * p.seg_items;
+    for (int u = j; u < span; u += R) {
+        const int li = u / nseg, sg = u - li * nseg;
+        const int it = sg * p.seg_items + li;
+        if (it >= total) continue;  // past the end of a shorter last segment
         if (leader) sh.verdict[0] = spin_until(sh, p.status, p.cnt + it, target) ? 1 : 0;
         __syncthreads();
         if (!*reinterpret_cast<volatile int*>(&sh.verdict[0])) break;
-        const float* src = p.part + static_cast<size_t>(it) * H2 * CH + t;
+        // the chunk's partials slot: its segment's ring, its place in the segment mod the ring
+        const float* src =
+            p.part + (static_cast<size_t>(sg) * kPartRing + li % kPartRing) * H2 * CH + t;
         float acc = 0.f;
         for (int k0 = lo; k0 < hi; k0 += 8) {
             float v[8];
@@ -336,7 +417,12 @@ __device__ void reducer(Shared& sh, float (*red)[CH], const Params& p, int j, in
             float tot = 0.f;
 #pragma unroll
             for (int g = 0; g < G; ++g) tot += red[g][t];
-            __stcg(p.rn + static_cast<size_t>(it) * CH + t, rsqrtf(tot * p.inv_width + p.eps));
+            const float r = rsqrtf(tot * p.inv_width + p.eps);
+            float* dst = p.rn + static_cast<size_t>(it) * CH + t;
+            if (t == 0)  // after the barrier above: every read of the chunk's partials is done
+                st_release_gpu_u32(reinterpret_cast<unsigned*>(dst), __float_as_uint(r));
+            else
+                __stcg(dst, r);
         }
         __syncthreads();  // red is rewritten by the next chunk
     }
@@ -360,9 +446,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();
     const uint32_t peer = rank ^ 1u;
-    const int h = blockIdx.x >> 1;
     const int H = p.H;
     const int total = p.total;                               // (sequence, chunk) iterations
+    const int cl = static_cast<int>(blockIdx.x >> 1);        // head pair index
+    const int h = cl % H, seg = cl / H;                      // head, segment of the items
+    const int it0 = seg * p.seg_items;                       // this pair's items: [it0, it0 + n_loc)
+    const int n_loc = (total - it0 < p.seg_items ? total - it0 : p.seg_items);
     const int col0 = h * D + static_cast<int>(rank) * DV;    // first feature column owned
     const uint32_t own_off = rank == 0 ? OFF_QB : OFF_KB;    // the tile this CTA activates
 
@@ -373,13 +462,15 @@ __global__ void __launch_bounds__(kThreads, 1)
              i += static_cast<int64_t>(gridDim.x) * kThreads)
             p.xch_clear[i] = e;
     }
-    if (static_cast<int>(blockIdx.x) >= 2 * H) {  // a reducer CTA (no TMEM, no cluster traffic)
+    const int heads2 = 2 * H * p.nseg;  // head CTAs; the reducer CTAs follow
+    if (static_cast<int>(blockIdx.x) >= heads2) {  // a reducer CTA (no TMEM, no cluster traffic)
         if (tid == 0) {
             sh.abort_flag = 0;
             sh.verdict[0] = 0;
         }
         __syncthreads();
-        reducer(sh, sh.red, p, static_cast<int>(blockIdx.x) - 2 * H, static_cast<int>(gridDim.x) - 2 * H);
+        reducer(sh, sh.red, p, static_cast<int>(blockIdx.x) - heads2,
+                static_cast<int>(gridDim.x) - heads2);
         return;
     }
 
@@ -425,8 +516,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // -------------------------------------------- TMA producer: q or k, and v
             const CUtensorMap* own_map = rank == 0 ? &tq : &tk;
             int issued = 0;
-            for (int it = 0; it < total; ++it) {
-                const Item im = item_at<kVarlen>(p, it);
+            for (int it = 0; it < n_loc; ++it) {
+                const Item im = item_at<kVarlen>(p, it0 + it);
                 const int s = it & 1;
                 const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
                 if (!wait_bar(sh, p.status, &sh.qkempty[s], ph ^ 1u)) break;
@@ -450,8 +541,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (lane == 1) {
             // -------------------------------------------- TMA producer: g
             int issued = 0;
-            for (int it = 0; it < total; ++it) {
-                const Item im = item_at<kVarlen>(p, it);
+            for (int it = 0; it < n_loc; ++it) {
+                const Item im = item_at<kVarlen>(p, it0 + it);
                 const int gs = it % kGBufs;
                 const uint32_t gph = static_cast<uint32_t>(it / kGBufs) & 1u;
                 if (!wait_bar(sh, p.status, &sh.gempty[gs], gph ^ 1u)) break;
@@ -464,8 +555,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
+            const uint64_t dq0 = desc_kmajor(sbase + OFF_QB, 0), dk0 = desc_kmajor(sbase + OFF_KB, 0);
+            const uint64_t dkm0 = desc_mnmajor(sbase + OFF_KB, 0);
+            const uint64_t dvm0 = desc_mnmajor(sbase + OFF_VB, 0);
+            const uint64_t ds0 = desc_mnmajor(sbase + OFF_SB, 0);
             int seen = 0;
-            for (int it = 0; it < total; ++it) {
+            for (int it = 0; it < n_loc; ++it) {
                 const int s = it & 1;
                 const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
                 const uint32_t par = static_cast<uint32_t>(it) & 1u;
@@ -474,8 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait_bar(sh, p.status, &sh.actdone[s], ph)) break;
                 if (!wait_bar(sh, p.status, &sh.xin[s], ph)) break;
                 seen = it + 1;
-                const uint32_t qa = sbase + OFF_QB + s * TILE, ka = sbase + OFF_KB + s * TILE;
-                const uint32_t va = sbase + OFF_VB + s * HALF, sb = sbase + OFF_SB;
+                const uint64_t dq = desc_add(dq0, s * TILE), dk = desc_add(dk0, s * TILE);
+                const uint64_t dkm = desc_add(dkm0, s * TILE), dvm = desc_add(dvm0, s * HALF);
                 const uint32_t tY = tm + TM_Y + yb * DV;
                 bool ok = true;
                 // scores A = Q^ K^T (128 x 128), once P V^ has read both halves of A
@@ -485,7 +580,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_ss(tm + TM_A, desc_kmajor(qa, ks), desc_kmajor(ka, ks), IDESC_QK, ks > 0);
+                    mma_ss(tm + TM_A, desc_add(dq, kofs(ks)), desc_add(dk, kofs(ks)), IDESC_QK,
+                           ks > 0);
                 mma_commit(&sh.afull[0]);
                 mma_commit(&sh.afull[1]);
                 if (!wait_bar(sh, p.status, &sh.yempty[yb], yph ^ 1u)) break;
@@ -494,11 +590,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Y = Q^ S_{<c}  (this CTA's 64 columns)
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_ss(tY, desc_kmajor(qa, ks), desc_mnmajor(sb, ks), IDESC_QS, ks > 0);
+                    mma_ss(tY, desc_add(dq, kofs(ks)), desc_add(ds0, ks * 2048), IDESC_QS, ks > 0);
                 // S += K^T V  (fp32 in TMEM)
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_ss(tm + TM_S, desc_mnmajor(ka, ks), desc_mnmajor(va, ks), IDESC_KV, 1u);
+                    mma_ss(tm + TM_S, desc_add(dkm, ks * 2048), desc_add(dvm, ks * 2048), IDESC_KV,
+                           1u);
                 mma_commit(&sh.sdone);
                 // q^ and k^ of this stage are no longer read (this CTA and the peer's copy)
                 mma_commit_multicast(&sh.qkempty[s], static_cast<uint16_t>(3u));
@@ -509,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
                         mma_ts(tY, tm + TM_A + 64 * j + ks * 8,
-                               desc_mnmajor(va + 8192 * j, ks), IDESC_PV, 1u);
+                               desc_add(dvm, 8192 * j + ks * 2048), IDESC_PV, 1u);
                     mma_commit(&sh.aempty[j]);
                 }
                 if (!ok) break;
@@ -528,14 +625,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool leader = tid == 128;
         const uint32_t peer_own = map_to_rank(sbase + own_off, peer);
         const uint32_t peer_xin = map_to_rank(smem_addr(&sh.xin[0]), peer);
-        for (int it = 0; it < total; ++it) {
+        for (int it = 0; it < n_loc; ++it) {
             const int s = it & 1;
             const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
             if (!group_wait(sh, p.status, &sh.rawqk[s], ph, leader, 1, 256, 0)) break;
             // rows past a packed sequence's end hold the next sequence's tokens and become
             // zero; in a uniform batch the rows past N are already the tensor map's zero
             // fill, and SiLU(0) = 0
-            const bool live = !kVarlen || t < p.items[it].y;
+            const bool live = !kVarlen || t < p.items[it0 + it].y;
             uint8_t* blk = sm + own_off + s * TILE + part * HALF;
             uint4 x[4];
             if (kAct && live) {
@@ -587,9 +684,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool leader = t == 0;
         const uint32_t lb = tm + (static_cast<uint32_t>(q4 * 32) << 16);
         uint8_t* sbk = sm + OFF_SB;
-        for (int it = 0; it <= total; ++it) {
-            const Item im = item_at<kVarlen>(p, it < total ? it : total - 1);
-            const bool first = it == total || im.first;  // a sequence ends before it
+        for (int it = 0; it <= n_loc; ++it) {
+            const Item im = item_at<kVarlen>(p, it0 + (it < n_loc ? it : n_loc - 1));
+            // a sequence (or this pair's segment) ends before it, or one starts at it
+            const bool first = it == n_loc || it == 0 || im.first;
             // (1) the bf16 operand S_{<c} for iteration it
             if (it > 0) {
                 if (!group_wait(sh, p.status, &sh.sdone, static_cast<uint32_t>(it - 1) & 1u,
@@ -598,42 +696,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
             }
             if (first) {
-                if (it > 0 && p.S_out) {  // the finished sequence's final state
-                    const int pb = item_at<kVarlen>(p, it - 1).b;
-                    float* dst = p.S_out + ((static_cast<size_t>(pb) * H + h) * D + t) * D +
-                                 rank * DV;
-#pragma unroll
-                    for (int part = 0; part < 2; ++part) {
-                        uint32_t r[32];
-                        LA_TMEM_LD32(lb + TM_S + 32 * part, r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<float4*>(dst + 32 * part + j) =
-                                make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                            __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-                    }
+                if (it > 0 && p.S_out && seg == p.nseg - 1) {  // a finished sequence's state
+                    const int pb = item_at<kVarlen>(p, it0 + it - 1).b;
+                    state_rows_out(p.S_out + ((static_cast<size_t>(pb) * H + h) * D + t) * D +
+                                       rank * DV,
+                                   lb + TM_S);
                 }
-                if (it == total) break;
+                if (it == n_loc) break;
+                // segment mode: every segment starts from its prefix state (the first's is
+                // a copy of S_in, so nothing reads S_in while the last segment writes S_out)
                 const float* src =
-                    p.S_in ? p.S_in + ((static_cast<size_t>(im.b) * H + h) * D + t) * D + rank * DV
-                           : nullptr;
-#pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    uint32_t r[32];
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        const float4 f = src ? *reinterpret_cast<const float4*>(src + 32 * part + j)
-                                             : make_float4(0.f, 0.f, 0.f, 0.f);
-                        r[j] = __float_as_uint(f.x);
-                        r[j + 1] = __float_as_uint(f.y);
-                        r[j + 2] = __float_as_uint(f.z);
-                        r[j + 3] = __float_as_uint(f.w);
-                    }
-                    LA_TMEM_ST32(lb + TM_S + 32 * part, r);
-                    store_row_bf16(sbk, t, part, r);
-                }
-                tmem_wait_st();
+                    p.S_seg  ? p.S_seg + ((static_cast<size_t>(seg) * H + h) * D + t) * D
+                    : p.S_in ? p.S_in + ((static_cast<size_t>(im.b) * H + h) * D + t) * D
+                             : nullptr;
+                state_rows_in(src ? src + rank * DV : nullptr, lb + TM_S, sbk, t);
             } else {
 #pragma unroll
                 for (int part = 0; part < 2; ++part) {
@@ -701,9 +777,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = q4 * 32 + lane;  // token row
         const bool leader = t == 0;
         const uint32_t lb = tm + (static_cast<uint32_t>(q4 * 32) << 16);
-        for (int it = 0; it < total; ++it) {
+        float* const ring = p.part + static_cast<size_t>(seg) * kPartRing * 2 * H * CH;
+        for (int it = 0; it < n_loc; ++it) {
             const int yb = it % kYBufs;
             const uint32_t yph = static_cast<uint32_t>(it / kYBufs) & 1u;
+            const int gi = it0 + it;  // the chunk's index in the whole list
+            if (it >= kPartRing) {
+                // the partials slot is reused: chunk gi - kPartRing's reducer has read it
+                // (the y ring makes this long done; the acquire orders the reuse)
+                const bool ok =
+                    !leader ||
+                    spin_published(sh, p.status, p.rn + static_cast<size_t>(gi - kPartRing) * CH);
+                if (!named_bar_and(3, 128, ok)) break;
+            }
             if (!group_wait(sh, p.status, &sh.yfull[yb], yph, leader, 3, 128, 2)) break;
             tc_fence_after();
             float ss0 = 0.f, ss1 = 0.f;
@@ -718,9 +804,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ss1 = fmaf(__uint_as_float(y[j + 1]), __uint_as_float(y[j + 1]), ss1);
                 }
             }
-            __stcg(p.part + (static_cast<size_t>(it) * 2 * H + 2 * h + rank) * CH + t, ss0 + ss1);
+            __stcg(ring + (static_cast<size_t>(it % kPartRing) * 2 * H + 2 * h + rank) * CH + t,
+                   ss0 + ss1);
             named_bar_sync(3, 128);
-            if (leader) red_release_gpu_add(p.cnt + it, 1u);  // orders the group's stores
+            if (leader) red_release_gpu_add(p.cnt + gi, 1u);  // orders the group's stores
         }
     } else if (warp >= 20) {
         // ------------------------------------------------ finish: norm, gate, store.  Both
@@ -734,8 +821,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t bar_id = 4 + fg;
         const int slot = 3 + fg;
         const uint32_t lb = tm + (static_cast<uint32_t>(q4 * 32) << 16);
-        for (int it = 0; it < total; ++it) {
-            const Item im = item_at<kVarlen>(p, it);
+        for (int it = 0; it < n_loc; ++it) {
+            const Item im = item_at<kVarlen>(p, it0 + it);
             const int yb = it % kYBufs;
             const uint32_t yph = static_cast<uint32_t>(it / kYBufs) & 1u;
             const int gs = it % kGBufs;
@@ -744,7 +831,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float rn = 0.f;
             bool ready = false;
             {
-                const float* src = p.rn + static_cast<size_t>(it) * CH + t;
+                const float* src = p.rn + static_cast<size_t>(it0 + it) * CH + t;
                 uint64_t t0 = 0;
                 for (;;) {
                     rn = __ldcg(src);
@@ -939,8 +1026,9 @@ size_t flag_words_for(int total) {
     return flag_cnt_words(total) + static_cast<size_t>(total) * CH;
 }
 
-int reducers_for(int H) {
-    const int spare = max_active_clusters() - H;
+// Reducer CTAs for `pairs` head pairs: the clusters left over, at most kMaxReducers / 2.
+int reducers_for(int pairs) {
+    const int spare = max_active_clusters() - pairs;
     const int clusters = spare < kMaxReducers / 2 ? spare : kMaxReducers / 2;
     return clusters > 0 ? 2 * clusters : 0;
 }
@@ -963,8 +1051,34 @@ int prefill_tc_supported(int B, int H, int64_t N) {
 
 size_t prefill_tc_flag_words(int items) { return flag_words_for(items); }
 
-size_t prefill_tc_part_floats(int items, int H) {
-    return static_cast<size_t>(items) * 2 * H * CH;
+size_t prefill_tc_part_floats(int H, int nseg) {
+    return static_cast<size_t>(nseg) * kPartRing * 2 * H * CH;
+}
+
+int prefill_tc_segment_plan(int B, int H, int64_t N, int* seg_items, int* fine) {
+    *seg_items = 0;
+    *fine = 1;
+    if (B != 1 || N <= 0) return 1;
+    const int64_t Nc = (N + CH - 1) / CH;
+    const int clusters = max_active_clusters();
+    if (clusters <= 1) return 1;
+    // head pairs of all segments plus the reducer pairs resident at once (the full set
+    // of kMaxReducers / 2 pairs when that still gives two segments, else one pair), and
+    // segments of at least kMinSegChunks chunks
+    int64_t nseg = (clusters - kMaxReducers / 2) / H;
+    if (nseg < 2) nseg = (clusters - 1) / H;
+    if (nseg > Nc / kMinSegChunks) nseg = Nc / kMinSegChunks;
+    if (nseg < 2) return 1;
+    // the state pass splits each prefix segment into m pieces so that it fills the SMs
+    int64_t m = static_cast<int64_t>(2 * clusters) / (static_cast<int64_t>(H) * (nseg - 1));
+    if (m < 1) m = 1;
+    const int64_t cps = (Nc + nseg * m - 1) / (nseg * m);  // chunks per piece
+    const int64_t per = cps * m;                            // chunks per segment
+    const int64_t used = (Nc + per - 1) / per;              // non-empty segments
+    if (used < 2) return 1;
+    *seg_items = static_cast<int>(per);
+    *fine = static_cast<int>(m);
+    return static_cast<int>(used);
 }
 
 int prefill_tc_items(int B, int64_t N) {
@@ -975,11 +1089,18 @@ namespace {
 
 // Launches the kernel over `total` items: B sequences of N tokens (items == nullptr) or
 // a packed batch viewed as one slab of N tokens (items: the per-item table on device).
+// nseg > 1 (B == 1, uniform): the items are cut into nseg runs of seg_items, each run by
+// its own H head pairs from the state S_seg[seg].
 int launch_items(const void* q, const void* k, const void* v, const void* g, void* out,
                  const float* S_in, float* S_out, float* y_debug, int B, int H, int64_t N,
                  int total, const int4* items, float eps, bool activated, const Workspace& ws,
-                 const XchLease& xl, cudaStream_t st) {
-    const int R = reducers_for(H);
+                 const XchLease& xl, cudaStream_t st, int nseg = 1, int seg_items = 0,
+                 const float* S_seg = nullptr) {
+    if (nseg < 1 || (nseg > 1 && (B != 1 || items || !S_seg))) return LA_ERR_INVALID_ARG;
+    if (nseg == 1) seg_items = total;
+    if (seg_items < 1 || static_cast<int64_t>(nseg - 1) * seg_items >= total)
+        return LA_ERR_INVALID_ARG;  // every segment holds at least one item
+    const int R = reducers_for(H * nseg);
     if (R <= 0) return LA_ERR_UNSUPPORTED;
     CUtensorMap mq, mk, mv, mg, mo;
     if (!encode_io_map(&mq, q, B, H, N) || !encode_io_map(&mk, k, B, H, N) ||
@@ -1004,10 +1125,13 @@ int launch_items(const void* q, const void* k, const void* v, const void* g, voi
     prm.Nc = static_cast<int>((N + CH - 1) / CH);
     prm.nc_magic = ~0ull / static_cast<uint64_t>(prm.Nc);
     prm.total = total;
+    prm.nseg = nseg;
+    prm.seg_items = seg_items;
+    prm.S_seg = S_seg;
     prm.eps = eps;
     prm.inv_width = 1.0f / static_cast<float>(H * D);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * H + R), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * H * nseg + R), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = SMEM_DYN;
     cfg.stream = st;
@@ -1041,10 +1165,10 @@ int launch_items(const void* q, const void* k, const void* v, const void* g, voi
 int launch_prefill_tc(const void* q, const void* k, const void* v, const void* g, void* out,
                       const float* S_in, float* S_out, float* y_debug, int B, int H, int64_t N,
                       float eps, bool activated, const Workspace& ws, const XchLease& xl,
-                      cudaStream_t st) {
+                      cudaStream_t st, int nseg, int seg_items, const float* S_seg) {
     const int total = static_cast<int>(static_cast<int64_t>(B) * ((N + CH - 1) / CH));
     return launch_items(q, k, v, g, out, S_in, S_out, y_debug, B, H, N, total, nullptr, eps,
-                        activated, ws, xl, st);
+                        activated, ws, xl, st, nseg, seg_items, S_seg);
 }
 
 int launch_prefill_tc_varlen(const void* q, const void* k, const void* v, const void* g,

@@ -45,6 +45,8 @@ WORKLOADS = {
     "attn_8k": Workload("attn_8k", 1, 64, 8192, 128, "bf16", 1.0, 8),
     # packed batch: 64K tokens in sequences of seeded lengths (varlen_lengths)
     "prefill_varlen_64k": Workload("prefill_varlen_64k", 1, 64, 65536, 128, "bf16", 0.5, 6),
+    # one long sequence with few heads (8 of 128): the segment-parallel prefill
+    "prefill_h8_256k": Workload("prefill_h8_256k", 1, 8, 262144, 128, "bf16", 0.5, 9),
 }
 
 

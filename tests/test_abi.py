@@ -84,8 +84,9 @@ def _prefill(lib, B=1, H=2, N=16, d=128, dtype=la.LA_BF16, eps=1e-6, flags=0, q=
     (dict(eps=-1.0), la.LA_ERR_INVALID_ARG),
     (dict(eps=float("nan")), la.LA_ERR_INVALID_ARG),
     (dict(flags=0x100), la.LA_ERR_INVALID_ARG),
-    (dict(flags=4), la.LA_ERR_INVALID_ARG),
+    (dict(flags=8), la.LA_ERR_INVALID_ARG),
     (dict(flags=la.LA_FLAG_ACTIVATED, d=64), la.LA_ERR_UNSUPPORTED),  # flag itself accepted
+    (dict(flags=la.LA_FLAG_SERIAL, d=64), la.LA_ERR_UNSUPPORTED),     # flag itself accepted
     (dict(q=ctypes.c_void_p(0)), la.LA_ERR_INVALID_ARG),
     (dict(q=MIS), la.LA_ERR_MISALIGNED),
     (dict(out=P[0]), la.LA_ERR_INVALID_ARG),           # out aliases q
@@ -164,6 +165,8 @@ def test_prefill_path_rejects_on_host(lib):
     assert lib.la_prefill_path(1, 1, 1, 128, 9, 0) == -la.LA_ERR_INVALID_ARG
     assert lib.la_prefill_path(1, 1, 1, 128, la.LA_F32, 0) == 1   # fp32: CUDA-core kernel
     assert lib.la_prefill_path(1, 1, 1, 128, la.LA_BF16, la.LA_FLAG_SIMT) == 1
+    assert lib.la_prefill_path(1, 1, 1, 128, la.LA_BF16, 8) == -la.LA_ERR_INVALID_ARG
+    assert lib.la_prefill_path(1, 1, 1, 128, la.LA_F32, la.LA_FLAG_SERIAL) == 1
 
 
 @pytest.mark.parametrize("cu,S,d,want", [

@@ -86,6 +86,13 @@ def test_tensor_core_path_selected(env):
         assert la.la_prefill_path(1, 64, N) == 0, N
     assert la.la_prefill_path(1, 64, 8192, simt=True) == 1
     assert la.la_prefill_path(1, 64, 8192, dtype=la.LA_F32) == 1
+    # one long sequence with few heads: the segment-parallel mode, unless asked not to
+    assert la.la_prefill_path(1, 8, 40000) == 2
+    assert la.la_prefill_path(1, 8, 40000, serial=True) == 0
+    assert la.la_prefill_path(2, 8, 40000) == 0       # only B == 1 is cut
+    assert la.la_prefill_path(1, 8, 16000) == 0       # under two segments of 64 chunks
+    assert la.la_prefill_path(1, 37, 1 << 20) == 0    # 2 x 37 head pairs do not fit
+    assert la.la_prefill_path(1, 36, 1 << 20) == 2
 
 
 def test_tiny_f32_workload(env):
@@ -125,6 +132,38 @@ def test_tensor_core_head_limit(env):
         la.la_prefill(q, k, v, g)
     assert e.value.status == la.LA_ERR_UNSUPPORTED
     _check_prefill(env, 1, 300, h_max + 1, "bf16", 0.5, 18, simt=True)
+
+
+@pytest.mark.parametrize("H,N,S0", [(8, 40000, False), (4, 33000, True), (16, 50000, False)])
+def test_segment_parallel_mode(env, H, N, S0):
+    """One long sequence with few heads runs as segments side by side (the blockwise
+    route's prefix over the d x d states), each from the state of the tokens before it;
+    out, y and the final state against the oracle.  N has a ragged last chunk."""
+    torch, la, _ = env
+    assert la.la_prefill_path(1, H, N) == 2
+    _check_prefill(env, 1, N, H, "bf16", 0.5, 700 + H, simt=False, S0=S0)
+
+
+def test_segment_parallel_mode_repeatable_and_in_place(env):
+    """The segment mode is deterministic, takes kv_state_out == kv_state_in, and agrees
+    with the serial chain to the parity tolerance (only the order of fp32 state
+    additions differs)."""
+    torch, la, _ = env
+    B, N, H = 1, 40000, 8
+    q, k, v, g = _inputs(torch, B, N, H, torch.bfloat16, 0.5, 811)
+    gen = torch.Generator(device="cuda").manual_seed(812)
+    S_in = torch.randn((B, H, 128, 128), generator=gen, device="cuda") * 0.5
+    out1, S1 = la.la_prefill(q, k, v, g, kv_state_in=S_in)
+    out2, S2 = la.la_prefill(q, k, v, g, kv_state_in=S_in)
+    S_io = S_in.clone()
+    out3, _ = la.la_prefill(q, k, v, g, kv_state_in=S_io, kv_state_out=S_io)
+    out_s, S_s = la.la_prefill(q, k, v, g, kv_state_in=S_in, serial=True)
+    torch.cuda.synchronize()
+    assert la.la_get_device_status() == 0
+    assert torch.equal(out1, out2) and torch.equal(S1, S2)
+    assert torch.equal(out3, out1) and torch.equal(S_io, S1)
+    assert rel_max_err(host64(out1), host64(out_s)) <= TOL["bf16"]["out"]
+    assert rel_max_err(host64(S1), host64(S_s)) <= TOL["bf16"]["state"]
 
 
 def test_prefill_8k_workload_full(env):
