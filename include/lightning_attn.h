@@ -147,8 +147,8 @@ int la_decode_step_ex(float* kv_state, const void* q, const void* k, const void*
    The segment-parallel mode is the blockwise route's prefix over the d x d states
    ("Hybrid Modeling": the O(d^2 n) form) spread over the SMs that a few heads leave
    idle.  It runs for one sequence (B == 1) when the device holds at least twice H
-   head pairs plus a reducer pair and N spans at least 2 x 8192 tokens, unless
-   LA_FLAG_SERIAL is set: the tokens are cut into segments of whole 128-token chunks,
+   head pairs plus a reducer pair (H <= 36 on a 148-SM B300) and N spans at least
+   2 x 64 chunks of 128 tokens (N > 16256), unless LA_FLAG_SERIAL is set: the tokens are cut into segments of whole 128-token chunks,
    the state-only pass (as la_state_pass) sums K^T V^ over the tokens before each
    segment, the per-segment states are added in a fixed order, and then every segment
    runs its own head pairs from its prefix state, all segments in one launch.  It reads

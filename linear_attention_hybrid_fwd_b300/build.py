@@ -48,6 +48,21 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+TIMELINE_LIB = os.path.join(PKG, "liblightning_attn_timeline.so")
+
+
+def build_timeline(force: bool = False) -> str:
+    """The same sources with -DLA_TIMELINE: the prefill kernel stamps its pipeline
+    events (see timeline.py).  A separate library; the product library is unchanged."""
+    if not force and os.path.exists(TIMELINE_LIB) and os.path.exists(LIB) and \
+            os.path.getmtime(TIMELINE_LIB) >= os.path.getmtime(build()):
+        return TIMELINE_LIB
+    tmp = TIMELINE_LIB + f".tmp{os.getpid()}"
+    subprocess.check_call([NVCC, *ARCH, *FLAGS, "-DLA_TIMELINE", *sources(), "-o", tmp])
+    os.replace(tmp, TIMELINE_LIB)
+    return TIMELINE_LIB
+
+
 if __name__ == "__main__":
     build(force="--force" in sys.argv, verbose="-v" in sys.argv)
     print(LIB)

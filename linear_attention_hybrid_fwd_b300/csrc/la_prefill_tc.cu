@@ -166,6 +166,24 @@ struct Shared {
     float red[kThreads / 128][CH];  // reducer: per-token sums over ranges of head halves
 };
 
+// Per-stage timeline (a build with -DLA_TIMELINE only): %globaltimer stamps of the
+// pipeline events of the first kTlChunks iterations of every CTA, read back with
+// la_timeline_fetch.  Event numbers are listed in linear_attention_hybrid_fwd_b300/timeline.py.
+#ifdef LA_TIMELINE
+constexpr int kTlCtas = 160, kTlChunks = 64, kTlEvents = 32;
+__device__ unsigned long long g_la_timeline[kTlCtas * kTlChunks * kTlEvents];
+__device__ __forceinline__ void tl_stamp(int it, int e) {
+    if (it >= 0 && it < kTlChunks && blockIdx.x < kTlCtas) {
+        unsigned long long t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        g_la_timeline[(blockIdx.x * kTlChunks + it) * kTlEvents + e] = t;
+    }
+}
+#define LA_TL(e) tl_stamp(it, (e))
+#else
+#define LA_TL(e) ((void)0)
+#endif
+
 // ------------------------------------------------------------------ numerics
 __device__ __forceinline__ float tanh_approx(float x) {
     float y;
@@ -399,6 +417,7 @@ __device__ void reducer(Shared& sh, float (*red)[CH], const Params& p, int j, in
         if (leader) sh.verdict[0] = spin_until(sh, p.status, p.cnt + it, target) ? 1 : 0;
         __syncthreads();
         if (!*reinterpret_cast<volatile int*>(&sh.verdict[0])) break;
+        if (tid == 0) LA_TL(25);
         // the chunk's partials slot: its segment's ring, its place in the segment mod the ring
         const float* src =
             p.part + (static_cast<size_t>(sg) * kPartRing + li % kPartRing) * H2 * CH + t;
@@ -423,6 +442,7 @@ __device__ void reducer(Shared& sh, float (*red)[CH], const Params& p, int j, in
                 st_release_gpu_u32(reinterpret_cast<unsigned*>(dst), __float_as_uint(r));
             else
                 __stcg(dst, r);
+            if (t == 0) LA_TL(26);
         }
         __syncthreads();  // red is rewritten by the next chunk
     }
@@ -525,11 +545,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(&sh.rawqk[s], TILE);
                 tma_load_3d(own, own_map, h * D, im.y, im.z, &sh.rawqk[s]);
                 tma_load_3d(own + HALF, own_map, h * D + 64, im.y, im.z, &sh.rawqk[s]);
+                LA_TL(0);
                 mbar_arrive_expect_tx(&sh.xin[s], TILE);  // the peer's activated tile
                 issued = it + 1;
                 if (!wait_bar(sh, p.status, &sh.vempty[s], ph ^ 1u)) break;
                 mbar_arrive_expect_tx(&sh.rawv[s], HALF);
                 tma_load_3d(sm + OFF_VB + s * HALF, &tv, col0, im.y, im.z, &sh.rawv[s]);
+                LA_TL(1);
             }
             sh.issued = issued;
             // drain: the last loads land before this CTA may exit
@@ -548,6 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait_bar(sh, p.status, &sh.gempty[gs], gph ^ 1u)) break;
                 mbar_arrive_expect_tx(&sh.gfull[gs], HALF);
                 tma_load_3d(sm + OFF_GB + gs * HALF, &tg, col0, im.y, im.z, &sh.gfull[gs]);
+                LA_TL(2);
                 issued = it + 1;
             }
             sh.g_issued = issued;
@@ -569,6 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait_bar(sh, p.status, &sh.actdone[s], ph)) break;
                 if (!wait_bar(sh, p.status, &sh.xin[s], ph)) break;
                 seen = it + 1;
+                LA_TL(7);
                 const uint64_t dq = desc_add(dq0, s * TILE), dk = desc_add(dk0, s * TILE);
                 const uint64_t dkm = desc_add(dkm0, s * TILE), dvm = desc_add(dvm0, s * HALF);
                 const uint32_t tY = tm + TM_Y + yb * DV;
@@ -577,6 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait_bar(sh, p.status, &sh.aempty[0], par ^ 1u) ||
                     !wait_bar(sh, p.status, &sh.aempty[1], par ^ 1u))
                     break;
+                LA_TL(27);
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
@@ -584,8 +609,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                            ks > 0);
                 mma_commit(&sh.afull[0]);
                 mma_commit(&sh.afull[1]);
+                LA_TL(8);
                 if (!wait_bar(sh, p.status, &sh.yempty[yb], yph ^ 1u)) break;
+                LA_TL(28);
                 if (!wait_bar(sh, p.status, &sh.sready, par)) break;
+                LA_TL(29);
                 tc_fence_after();
                 // Y = Q^ S_{<c}  (this CTA's 64 columns)
 #pragma unroll
@@ -599,9 +627,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&sh.sdone);
                 // q^ and k^ of this stage are no longer read (this CTA and the peer's copy)
                 mma_commit_multicast(&sh.qkempty[s], static_cast<uint16_t>(3u));
+                LA_TL(9);
                 // Y += P_j V^_j, P_j = mask(A_j) in bf16 over the first 32 columns of A_j
                 for (int j = 0; j < 2 && ok; ++j) {
                     if (!wait_bar(sh, p.status, &sh.pfull[j], par)) { ok = false; break; }
+                    LA_TL(30 + j);
                     tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
@@ -612,6 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 mma_commit(&sh.yfull[yb]);
                 mma_commit(&sh.vempty[s]);
+                LA_TL(10);
             }
             sh.xin_seen = seen;
             mma_commit(&sh.mmadone);
@@ -629,6 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = it & 1;
             const uint32_t ph = static_cast<uint32_t>(it >> 1) & 1u;
             if (!group_wait(sh, p.status, &sh.rawqk[s], ph, leader, 1, 256, 0)) break;
+            if (leader) LA_TL(3);
             // rows past a packed sequence's end hold the next sequence's tokens and become
             // zero; in a uniform batch the rows past N are already the tensor map's zero
             // fill, and SiLU(0) = 0
@@ -654,10 +686,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_proxy_async_smem();
             named_bar_sync(1, 256);
+            if (leader) LA_TL(4);
             if (leader)
                 bulk_copy_to_peer(peer_own + s * TILE, sbase + own_off + s * TILE, TILE,
                                   peer_xin + s * 8);
             if (!group_wait(sh, p.status, &sh.rawv[s], ph, leader, 1, 256, 0)) break;
+            if (leader) LA_TL(5);
             uint8_t* vt = sm + OFF_VB + s * HALF;
             if (kAct && live) {
             } else if (live) {
@@ -676,6 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             named_bar_sync(1, 256);
             if (leader) mbar_arrive(&sh.actdone[s]);
+            if (leader) LA_TL(6);
         }
     } else if (warp >= 12 && warp < 16) {
         // ------------------------------------------------ state conversion + mask
@@ -695,6 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 tc_fence_after();
             }
+            if (leader && it < n_loc) LA_TL(11);
             if (first) {
                 if (it > 0 && p.S_out && seg == p.nseg - 1) {  // a finished sequence's state
                     const int pb = item_at<kVarlen>(p, it0 + it - 1).b;
@@ -723,6 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             named_bar_sync(2, 128);
             if (leader) mbar_arrive(&sh.sready);
+            if (leader) LA_TL(12);
             // (2) P_j = A_j masked to s <= t, bf16, over the first 32 columns of A_j
             bool ok = true;
             for (int j = 0; j < 2; ++j) {
@@ -732,6 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
+                if (leader) LA_TL(13 + 2 * j);
                 const uint32_t tA = lb + TM_A + 64 * j;
 #pragma unroll
                 for (int part = 0; part < 2; ++part) {
@@ -767,6 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 named_bar_sync(2, 128);
                 if (leader) mbar_arrive(&sh.pfull[j]);
+                if (leader) LA_TL(14 + 2 * j);
             }
             if (!ok) break;
         }
@@ -791,6 +830,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!named_bar_and(3, 128, ok)) break;
             }
             if (!group_wait(sh, p.status, &sh.yfull[yb], yph, leader, 3, 128, 2)) break;
+            if (leader) LA_TL(17);
             tc_fence_after();
             float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
@@ -808,6 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    ss0 + ss1);
             named_bar_sync(3, 128);
             if (leader) red_release_gpu_add(p.cnt + gi, 1u);  // orders the group's stores
+            if (leader) LA_TL(18);
         }
     } else if (warp >= 20) {
         // ------------------------------------------------ finish: norm, gate, store.  Both
@@ -851,9 +892,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!named_bar_and(bar_id, 128, ready)) break;
+            if (leader) LA_TL(19 + 3 * fg);
             // out = y (fp32, TMEM) * r_t * sigmoid(g), written over the g tile, then stored
             if (!group_wait(sh, p.status, &sh.gfull[gs], gph, leader, bar_id, 128, slot)) break;
             if (!group_wait(sh, p.status, &sh.yfull[yb], yph, leader, bar_id, 128, slot)) break;
+            if (leader) LA_TL(20 + 3 * fg);
             tc_fence_after();
             uint8_t* gt = sm + OFF_GB + gs * HALF;
             const float hrn = 0.5f * rn;
@@ -910,6 +953,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4*>(gt + swz(t, 4 * fg + j)) = gv[j];
             fence_proxy_async_smem();
             named_bar_sync(6, 256);  // both halves of the tile are written
+            if (leader) LA_TL(21 + 3 * fg);
             if (leader2) {
                 tma_store_3d(&to, gt, col0, im.y, im.z);  // rows past N are dropped
                 bulk_commit_group();
@@ -1181,3 +1225,15 @@ int launch_prefill_tc_varlen(const void* q, const void* k, const void* v, const 
 }
 
 }  // namespace la
+
+#ifdef LA_TIMELINE
+// Timeline builds only (not part of the public interface): copy the stamps to host
+// memory, or zero them.  Return a cudaError_t.
+extern "C" int la_timeline_fetch(void* host, size_t bytes) {
+    return static_cast<int>(cudaMemcpyFromSymbol(host, la::g_la_timeline, bytes));
+}
+extern "C" int la_timeline_clear() {
+    static unsigned long long zeros[la::kTlCtas * la::kTlChunks * la::kTlEvents];
+    return static_cast<int>(cudaMemcpyToSymbol(la::g_la_timeline, zeros, sizeof(zeros)));
+}
+#endif
