@@ -303,9 +303,9 @@ int la_prefill_ex(const void* q, const void* k, const void* v, const void* g, vo
             float* prefix = pieces + (size_t)(nseg - 1) * fine * set_floats;
             const int64_t Np = (int64_t)(nseg - 1) * seg_items * 128;
             rc = launch_state_tc(k, v, pieces, 1, H, Np, (nseg - 1) * fine, act, ws.status, st);
-            for (int s = 0; s < nseg && rc == LA_OK; ++s)
-                rc = launch_sum_rows(pieces, s * fine, (int64_t)set_floats, kv_state_in,
-                                     prefix + (size_t)s * set_floats, st);
+            if (rc == LA_OK)
+                rc = launch_prefix_rows(pieces, fine, nseg, (int64_t)set_floats, kv_state_in,
+                                        prefix, st);
             if (rc != LA_OK) return rc;
             S_seg = prefix;
         }

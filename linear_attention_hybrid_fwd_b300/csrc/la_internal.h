@@ -113,5 +113,9 @@ int launch_state_tc(const void* k, const void* v, float* part, int B, int H, int
 // out[j] = (base ? base[j] : 0) + sum_{i < count} parts[i * n + j] in the order of i.
 int launch_sum_rows(const float* parts, int count, int64_t n, const float* base, float* out,
                     cudaStream_t st);
+// out[s] = (base or 0) + sum_{i < s * per} parts[i] for s < nout, one running sum in the
+// order of i (each equal to launch_sum_rows with count = s * per).
+int launch_prefix_rows(const float* parts, int per, int nout, int64_t n, const float* base,
+                       float* out, cudaStream_t st);
 
 }  // namespace la

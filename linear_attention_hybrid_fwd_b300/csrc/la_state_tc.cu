@@ -286,6 +286,31 @@ __global__ void __launch_bounds__(256) k_sum_rows(const float* __restrict__ part
     }
 }
 
+// The prefixes of a segment-parallel prefill in one pass: out[s][j] = (base ? base[j] :
+// 0) + sum_{i < s * per} parts[i][j] for s = 0 .. nout - 1, each the same running sum,
+// in the order of i, that k_sum_rows forms for count = s * per (bitwise the same).
+__global__ void __launch_bounds__(256) k_prefix_rows(const float* __restrict__ parts, int per,
+                                                     int nout, int64_t n, const float* base,
+                                                     float* out) {
+    const int64_t n4 = n / 4;
+    for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < n4;
+         j += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        float4 acc = base ? reinterpret_cast<const float4*>(base)[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s = 0; s < nout; ++s) {
+            reinterpret_cast<float4*>(out + static_cast<size_t>(s) * n)[j] = acc;
+            if (s + 1 == nout) break;
+            for (int i = s * per; i < (s + 1) * per; ++i) {
+                const float4 x =
+                    __ldcs(reinterpret_cast<const float4*>(parts + static_cast<size_t>(i) * n) + j);
+                acc.x += x.x;
+                acc.y += x.y;
+                acc.z += x.z;
+                acc.w += x.w;
+            }
+        }
+    }
+}
+
 int g_num_sms[64];
 
 int num_sms() {
@@ -320,6 +345,19 @@ int launch_sum_rows(const float* parts, int count, int64_t n, const float* base,
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     k_sum_rows<<<static_cast<unsigned>(blocks), 256, 0, st>>>(parts, count, n, base, out);
+    if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
+    note_launches(1);
+    return LA_OK;
+}
+
+int launch_prefix_rows(const float* parts, int per, int nout, int64_t n, const float* base,
+                       float* out, cudaStream_t st) {
+    const int64_t n4 = n / 4;
+    int64_t blocks = (n4 + 255) / 256;
+    const int64_t cap = 8 * static_cast<int64_t>(num_sms());
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    k_prefix_rows<<<static_cast<unsigned>(blocks), 256, 0, st>>>(parts, per, nout, n, base, out);
     if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
     note_launches(1);
     return LA_OK;
