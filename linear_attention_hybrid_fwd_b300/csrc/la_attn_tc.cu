@@ -20,7 +20,7 @@
 //    once and the key/value tiles of the causal range into two stages by TMA (128B
 //    swizzle); the two query tiles share every key/value tile.  Warp 1 lane 0 issues
 //    tcgen05 MMAs: S_t = Q_t K_j^T (128 x 128, fp32) into query tile t's TMEM score
-//    buffer, and O_t += P_t V_j (P in TMEM, bf16) as two 64-column halves, followed at
+//    buffer, and O_t += P_t V_j (P in TMEM, bf16) as one N = 128 chain, followed at
 //    once by S_t of the next key tile.  Warps 4-7 (tile 0) and 8-11 (tile 1) own one
 //    query row per thread: they read S_t from TMEM, mask it (causal, keys past N),
 //    keep the running max m and sum l of the online softmax in base 2, write P_t as
@@ -65,7 +65,7 @@ constexpr uint32_t SMEM_DYN = SMEM_USED + 1024;       // + alignment slack
 static_assert(SMEM_DYN + 1024 <= 227 * 1024, "shared memory budget");
 constexpr uint32_t TM_S = 0, TM_O = 256;
 constexpr uint32_t IDESC_S = idesc_bf16_f32(BQ, BKV, 0, 0);   // Q K-major, K K-major
-constexpr uint32_t IDESC_PV = idesc_bf16_f32(BQ, 64, 0, 1);   // P (TMEM), V MN-major
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(BQ, D, 0, 1);    // P (TMEM), V MN-major, N = 128
 constexpr float kMaxSlack = 8.0f;      // base-2 growth of a row's max before O rescales
 constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s
 constexpr uint64_t kDrainNs = 200000000ull;     // 0.2 s
@@ -300,12 +300,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
 #pragma unroll
-                    for (int half = 0; half < 2; ++half)
-#pragma unroll
-                        for (int ks = 0; ks < BKV / 16; ++ks)
-                            mma_ts(tm + TM_O + t * BKV + 64 * half, tm + TM_S + t * BKV + ks * 8,
-                                   desc_mnmajor(va + half * HALF, ks), IDESC_PV,
-                                   (j > 0 || ks > 0) ? 1u : 0u);
+                    for (int ks = 0; ks < BKV / 16; ++ks)
+                        mma_ts(tm + TM_O + t * BKV, tm + TM_S + t * BKV + ks * 8,
+                               desc_mnmajor(va, ks), IDESC_PV, (j > 0 || ks > 0) ? 1u : 0u);
                     mma_commit(&sh.pvdone[t]);
                     if (j + 1 <= q0 + t) {
                         // the score buffer holds P_t until this product is done
