@@ -9,19 +9,25 @@
 // into four [T][H][d] bf16 tensors: exactly the inputs la_prefill reads.  The rows of W
 // are the q, k, v and g output features in that order (a fused nn.Linear weight).
 //
-// Design (one CTA per SM, persistent):
-//  * Output tiles of 128 tokens x 256 features; with H*d a multiple of 256 a tile lies
-//    in one of the four outputs.  Tiles are visited in groups of 16 token blocks, the
-//    token block fastest, so the CTAs working at one time share a few weight panels and
-//    the x panel of the group stays in L2.
-//  * Warp 0 lane 0 streams 64-wide K slices of the x tile (128 x 64) and the W tile
-//    (256 x 64) by TMA into a 4-stage ring of 48 KiB stages (128B swizzle).  Warp 1
-//    lane 0 issues tcgen05.mma (kind::f16, M = 128, N = 256, K = 16, fp32 accumulate)
-//    into one of two 256-column TMEM accumulators and frees each stage with a commit.
-//  * Warps 2-5 drain the other accumulator while the next tile accumulates: tcgen05.ld
-//    of 32 columns per thread (one token row each), SiLU for q, k, v, RNE to bf16 and
-//    four 16-byte stores per row and slice.  Rows past T are not stored (loads past T
-//    or past hidden read the tensor maps' zero fill, which adds nothing).
+// Design (two-CTA clusters, one CTA per SM, persistent):
+//  * Output tiles of 256 tokens x 256 features, one per CTA pair; with H*d a multiple of
+//    256 a tile lies in one of the four outputs.  Tiles are visited in groups of 8 pair
+//    rows (16 token blocks of 128), the token rows fastest, so the pairs working at one
+//    time share a few weight panels and the x panel of the group stays in L2.
+//  * The pair runs one M = 256 tcgen05.mma (cta_group::2, kind::f16, N = 256, K = 16,
+//    fp32 accumulate): each CTA holds its 128 token rows of the x tile and 128 of the
+//    256 weight rows, so a 64-wide K slice costs a CTA 32 KiB of shared memory instead
+//    of 48, and six stages fit.  Warp 0 lane 0 of each CTA streams its two halves by
+//    TMA (128B swizzle, cta_group::2) whose bytes complete on the even CTA's stage
+//    barrier; only the even CTA announces the stage's bytes (both CTAs' share), since a
+//    remote release-arrival from the odd CTA per stage measured 2x slower; warp 1 lane
+//    0 of the even CTA issues the MMAs into one of two 256-column TMEM accumulators
+//    (each CTA receives its 128 rows) and frees each stage in both CTAs with one commit.
+//  * Warps 2-5 of each CTA drain the other accumulator while the next tile accumulates:
+//    tcgen05.ld of 32 columns per thread (one token row each), SiLU for q, k, v, RNE to
+//    bf16 and four 16-byte stores per row and slice, then a release arrival on the even
+//    CTA's accumulator barrier.  Rows past T are not stored (loads past T or past hidden
+//    read the tensor maps' zero fill, which adds nothing).
 //  * SiLU(x) = x/2 (1 + tanh(x/2)) with the hardware tanh approximation, in fp32 on
 //    the fp32 accumulator.
 //  * Every wait is bounded (%globaltimer); a CTA that gives up records LA_ERR_TIMEOUT
@@ -43,18 +49,19 @@ namespace {
 
 using namespace sm100;
 
-constexpr int BM = 128;                 // tokens per tile (TMEM lanes)
+constexpr int BM = 128;                 // token rows per CTA (TMEM lanes); a pair: 256
 constexpr int BN = 256;                 // output features per tile (TMEM columns)
+constexpr int BNH = BN / 2;             // weight rows per CTA
 constexpr int BK = 64;                  // K per stage: one 128-byte swizzle row
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kThreads = 192;           // 6 warps
-constexpr int kGroupM = 16;             // token blocks per rasterisation group
+constexpr int kGroupM = 8;              // pair rows (256 tokens) per rasterisation group
 constexpr uint32_t A_BYTES = BM * BK * 2;             // 16 KiB
-constexpr uint32_t B_BYTES = BN * BK * 2;             // 32 KiB
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KiB
+constexpr uint32_t B_BYTES = BNH * BK * 2;            // 16 KiB
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KiB per CTA
 constexpr uint32_t SMEM_DYN = kStages * STAGE_BYTES + 1024;  // + alignment slack
 static_assert(SMEM_DYN + 1024 <= 227 * 1024, "shared memory budget");
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, 0, 0);  // A and B K-major
+constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN, 0, 0);  // M = 256, A and B K-major
 constexpr uint64_t kTimeoutNs = 4000000000ull;  // 4 s
 constexpr uint64_t kDrainNs = 200000000ull;     // 0.2 s
 
@@ -63,15 +70,17 @@ struct Params {
     int* status;
     int T;                  // tokens
     int HD;                 // H * d
-    int Mt, Nt, Kb;         // token blocks, feature blocks (of all four outputs), K slices
+    int Mt, Nt, Kb;         // pair rows (256 tokens), feature blocks (all four outputs), K slices
     int tiles;              // Mt * Nt
     int activate;           // SiLU on q, k, v
 };
 
 struct Shared {
+    // full, tempty, mmadone: used in the even CTA only
     uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], mmadone;
     uint32_t tmem_base;
     int abort_flag;
+    int issued[2];          // per CTA of the pair: stage loads issued (even CTA's copy)
 };
 
 __device__ __forceinline__ float tanh_approx(float x) {
@@ -92,14 +101,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ bool abort_set(Shared& sh) {
     return *reinterpret_cast<volatile int*>(&sh.abort_flag) != 0;
 }
-// Bounded wait for the phase of `bar` with `parity`; false when the CTA is aborting
+// Bounded wait for the phase of `bar` with `parity` (acquire at cluster scope when
+// kCluster: the arrivals come from the other CTA); false when the CTA is aborting
 // (honor_abort) or after `limit_ns`, in which case it raises the abort itself.
+template <bool kCluster = false>
 __device__ bool wait_bar(Shared& sh, int* status, uint64_t* bar, uint32_t parity,
                          bool honor_abort = true, uint64_t limit_ns = kTimeoutNs) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto probe = [&]() {
+        return kCluster ? mbar_try_wait_acq_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    };
+    if (probe()) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (probe()) return true;
         if ((it & 15u) == 0) {
             if (honor_abort && abort_set(sh)) return false;
             if (global_timer_ns() - t0 > limit_ns) {
@@ -111,8 +125,8 @@ __device__ bool wait_bar(Shared& sh, int* status, uint64_t* bar, uint32_t parity
     }
 }
 
-// Tile t -> (token block m, feature block n): groups of kGroupM token blocks, the token
-// block fastest within a group.
+// Tile t -> (pair row m, feature block n): groups of kGroupM pair rows, the pair row
+// fastest within a group.
 __device__ __forceinline__ void tile_mn(const Params& p, int t, int& m, int& n) {
     const int per_group = kGroupM * p.Nt;
     const int grp = t / per_group;
@@ -132,32 +146,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_addr(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int pair = static_cast<int>(blockIdx.x >> 1), npairs = static_cast<int>(gridDim.x >> 1);
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&sh.full[s], 1);
-            mbar_init(&sh.empty[s], 1);
+            mbar_init(&sh.full[s], 1);   // the even CTA's expect_tx for both CTAs' bytes
+            mbar_init(&sh.empty[s], 1);  // the pair MMA's commit
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&sh.tfull[a], 1);
-            mbar_init(&sh.tempty[a], 4);  // one arrival per epilogue warp
+            mbar_init(&sh.tempty[a], 8);  // one arrival per epilogue warp of both CTAs
         }
         mbar_init(&sh.mmadone, 1);
         sh.abort_flag = 0;
+        sh.issued[0] = sh.issued[1] = 0;
         fence_mbar_init();
     }
-    if (warp == 2) tmem_alloc(&sh.tmem_base, 512);
+    if (warp == 2) tmem_alloc_pair(&sh.tmem_base, 512);
     tc_fence_before();
     __syncthreads();
+    cluster_sync();  // both CTAs' barriers are initialised before any remote arrival
     tc_fence_after();
     const uint32_t tm = sh.tmem_base;
 
     if (warp == 0) {
         if (lane == 0) {
             // -------------------------------------------------------- TMA producer
+            // this CTA's 128 token rows and 128 weight rows of each stage, signalled on
+            // the even CTA's stage barrier
+            const uint32_t full0 = map_to_rank(smem_addr(&sh.full[0]), 0);
             int it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
+            for (int t = pair; t < p.tiles && ok; t += npairs) {
                 int m, n;
                 tile_mn(p, t, m, n);
                 for (int kb = 0; kb < p.Kb; ++kb) {
@@ -168,32 +189,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     uint8_t* st = sm + s * STAGE_BYTES;
-                    mbar_arrive_expect_tx(&sh.full[s], STAGE_BYTES);
-                    tma_load_3d(st, &tx, kb * BK, m * BM, 0, &sh.full[s]);
-                    tma_load_3d(st + A_BYTES, &tw, kb * BK, n * BN, 0, &sh.full[s]);
+                    const uint32_t fb = full0 + static_cast<uint32_t>(s) * 8u;
+                    // the even CTA announces both CTAs' bytes; the odd CTA's copies only
+                    // complete their share (a count that may run ahead of the announcement)
+                    if (rank == 0) mbar_arrive_expect_tx(&sh.full[s], 2 * STAGE_BYTES);
+                    tma_load_3d_pair(st, &tx, kb * BK, m * 2 * BM + static_cast<int>(rank) * BM, 0,
+                                     fb);
+                    tma_load_3d_pair(st + A_BYTES, &tw, kb * BK, n * BN + static_cast<int>(rank) * BNH,
+                                     0, fb);
                     ++it;
                 }
             }
-            // the last loads land before this CTA may exit
-            for (int j = it - kStages < 0 ? 0 : it - kStages; j < it; ++j)
-                wait_bar(sh, p.status, &sh.full[j % kStages],
-                         static_cast<uint32_t>(j / kStages) & 1u, false, kDrainNs);
+            // the even CTA drains both producers' loads (its stage barriers count them)
+            st_cluster_s32(map_to_rank(smem_addr(&sh.issued[rank]), 0), it);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // -------------------------------------------------------- MMA issuer
+        if (lane == 0 && rank == 0) {
+            // -------------------------------------------------------- MMA issuer (even CTA)
             int it = 0, ti = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x, ++ti) {
+            for (int t = pair; t < p.tiles && ok; t += npairs, ++ti) {
                 const int a = ti & 1;
                 const uint32_t aph = static_cast<uint32_t>(ti >> 1) & 1u;
-                if (!wait_bar(sh, p.status, &sh.tempty[a], aph ^ 1u)) break;
+                if (!wait_bar<true>(sh, p.status, &sh.tempty[a], aph ^ 1u)) break;
                 tc_fence_after();
                 const uint32_t acc = tm + static_cast<uint32_t>(a * BN);
                 for (int kb = 0; kb < p.Kb; ++kb, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = static_cast<uint32_t>(it / kStages) & 1u;
-                    if (!wait_bar(sh, p.status, &sh.full[s], ph)) {
+                    if (!wait_bar<true>(sh, p.status, &sh.full[s], ph)) {
                         ok = false;
                         break;
                     }
@@ -201,23 +225,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sa = sbase + s * STAGE_BYTES, sb = sa + A_BYTES;
 #pragma unroll
                     for (int ks = 0; ks < BK / 16; ++ks)
-                        mma_ss(acc, smem_desc_sw128(sa + ks * 32, 16, 1024),
-                               smem_desc_sw128(sb + ks * 32, 16, 1024), IDESC,
-                               (kb | ks) != 0 ? 1u : 0u);
-                    mma_commit(&sh.empty[s]);
+                        mma_ss_pair(acc, smem_desc_sw128(sa + ks * 32, 16, 1024),
+                                    smem_desc_sw128(sb + ks * 32, 16, 1024), IDESC,
+                                    (kb | ks) != 0 ? 1u : 0u);
+                    mma_commit_pair(&sh.empty[s], static_cast<uint16_t>(3u));
                 }
                 if (!ok) break;
-                mma_commit(&sh.tfull[a]);
+                mma_commit_pair(&sh.tfull[a], static_cast<uint16_t>(3u));
             }
-            mma_commit(&sh.mmadone);
+            mma_commit_pair(&sh.mmadone, static_cast<uint16_t>(1u));
             wait_bar(sh, p.status, &sh.mmadone, 0, false, kDrainNs);
         }
     } else {
         // ------------------------------------------------------------ epilogue (warps 2-5)
         const int quarter = warp & 3;  // TMEM lanes 32 quarter .. 32 quarter + 31
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t tempty0 = map_to_rank(smem_addr(&sh.tempty[0]), 0);
         int ti = 0;
-        for (int t = blockIdx.x; t < p.tiles; t += gridDim.x, ++ti) {
+        for (int t = pair; t < p.tiles; t += npairs, ++ti) {
             const int a = ti & 1;
             const uint32_t aph = static_cast<uint32_t>(ti >> 1) & 1u;
             const bool got = wait_bar(sh, p.status, &sh.tfull[a], aph);
@@ -229,7 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int seg = f0 / p.HD;        // 0 q, 1 k, 2 v, 3 g
             const int col0 = f0 - seg * p.HD;
             const bool act = p.activate != 0 && seg < 3;
-            const int64_t row = static_cast<int64_t>(m) * BM + quarter * 32 + lane;
+            const int64_t row = static_cast<int64_t>(m) * 2 * BM + static_cast<int>(rank) * BM +
+                                quarter * 32 + lane;
             const bool live = row < p.T;
             __nv_bfloat16* base =
                 seg == 0 ? p.out[0] : seg == 1 ? p.out[1] : seg == 2 ? p.out[2] : p.out[3];
@@ -259,19 +285,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.tempty[a]);
+            if (lane == 0) mbar_arrive_remote(tempty0 + static_cast<uint32_t>(a) * 8u);
         }
     }
+    // teardown: the even CTA waits for any stage the producers filled but the MMAs did
+    // not take (abort paths only), then both leave together
+    tc_fence_before();
     __syncthreads();
+    cluster_sync();  // both producers published their counts
+    if (rank == 0 && tid == 0) {
+        const int n = sh.issued[0] > sh.issued[1] ? sh.issued[0] : sh.issued[1];
+        for (int it = n - kStages < 0 ? 0 : n - kStages; it < n; ++it)
+            wait_bar(sh, p.status, &sh.full[it % kStages], static_cast<uint32_t>(it / kStages) & 1u,
+                     false, kDrainNs);
+    }
+    __syncthreads();
+    cluster_sync();  // no copy, MMA or arrival targets a CTA that has left
     tc_fence_after();
-    if (warp == 2) tmem_dealloc(tm, 512);
+    if (warp == 2) tmem_dealloc_pair(tm, 512);
 }
 
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 std::mutex g_dev_mutex;
-int g_sms[64];         // per device: SM count (0 = not queried yet)
+int g_sms[64];         // per device: co-resident two-CTA clusters (0 = not queried yet)
 bool g_attr_set[64];   // per device: the kernel's shared-memory attribute is set
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
@@ -304,20 +342,12 @@ bool encode_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, i
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// SM count of the current device, with the kernel's shared-memory attribute set; 0 on
-// failure.
+// Two-CTA clusters of the kernel that the current device holds at once, with the
+// kernel's shared-memory attribute set; 0 on failure.
 int prepare_device() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     std::lock_guard<std::mutex> lock(g_dev_mutex);
-    if (!g_sms[dev]) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-            cudaGetLastError();
-            return 0;
-        }
-        g_sms[dev] = n;
-    }
     if (!g_attr_set[dev]) {
         if (cudaFuncSetAttribute(k_qkvg_proj, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(SMEM_DYN)) != cudaSuccess) {
@@ -325,6 +355,25 @@ int prepare_device() {
             return 0;
         }
         g_attr_set[dev] = true;
+    }
+    if (!g_sms[dev]) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = SMEM_DYN;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = 2;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, k_qkvg_proj, &cfg) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            return 0;
+        }
+        g_sms[dev] = n;
     }
     return g_sms[dev];
 }
@@ -370,27 +419,41 @@ extern "C" int la_qkvg_projection(const void* x, const void* w, void* q, void* k
     }
     if (T == 0) return LA_OK;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(cuda_stream);
-    const int sms = prepare_device();
-    if (sms <= 0) return LA_ERR_CUDA;
+    const int pairs = prepare_device();
+    if (pairs <= 0) return LA_ERR_CUDA;
     Workspace ws;
     int rc = workspace_acquire(0, st, &ws);
     if (rc != LA_OK) return rc;
     CUtensorMap mx, mw;
-    if (!encode_rows(&mx, x, T, hidden, BM) || !encode_rows(&mw, w, int64_t(4) * HD, hidden, BN))
+    if (!encode_rows(&mx, x, T, hidden, BM) || !encode_rows(&mw, w, int64_t(4) * HD, hidden, BNH))
         return LA_ERR_UNSUPPORTED;
     Params prm;
     for (int i = 0; i < 4; ++i) prm.out[i] = static_cast<__nv_bfloat16*>(outs[i]);
     prm.status = ws.status;
     prm.T = static_cast<int>(T);
     prm.HD = HD;
-    prm.Mt = static_cast<int>((T + BM - 1) / BM);
+    prm.Mt = static_cast<int>((T + 2 * BM - 1) / (2 * BM));
     prm.Nt = 4 * HD / BN;
     prm.Kb = (hidden + BK - 1) / BK;
     prm.tiles = prm.Mt * prm.Nt;
     prm.activate = (flags & LA_PROJ_SILU) ? 1 : 0;
-    const int grid = prm.tiles < sms ? prm.tiles : sms;
-    k_qkvg_proj<<<grid, kThreads, SMEM_DYN, st>>>(mx, mw, prm);
-    if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
+    const int npairs = prm.tiles < pairs ? prm.tiles : pairs;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * npairs), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_DYN;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, k_qkvg_proj, mx, mw, prm) != cudaSuccess) {
+        cudaGetLastError();
+        return LA_ERR_CUDA;
+    }
     note_launches(1);
     return LA_OK;
 }
